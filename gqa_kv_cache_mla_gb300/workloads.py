@@ -1,0 +1,390 @@
+"""Seeded synthetic inputs for the fused KV-cache write path.
+
+This module only draws inputs: ragged request lengths, page tables, cache
+contents, activations, RMSNorm weights and the precomputed RoPE table that a
+serving engine would hand to the three entry points.  It contains none of the
+arithmetic of the path itself (no rotation, normalisation or quantisation);
+both the CUDA path and the CPU oracle consume exactly the arrays built here.
+
+All arrays are host numpy arrays.  bf16 values are carried as ``uint16`` bit
+patterns, FP8 cache bytes as ``uint8``.  The same seed gives the same bytes.
+
+Workloads (sizes and value distributions follow the five benchmark shapes of
+the MLA / GQA / K-cache RMSNorm pages):
+
+* ``mla_tiny``     2 requests, new [3,5], prior [0,7], 4 q heads, page 16
+* ``mla_decode``   DeepSeek-V3 decode: 256 requests x 1 token, prior U[1,8192]
+* ``mla_prefill``  16 requests, new U[512,8192], 1% outliers x20
+* ``gqa_llama3``   Llama-3-8B: 32 q / 8 kv heads, head 128, 32 requests
+* ``knorm``        8 kv heads, head 128, page 64, 64 mixed decode/prefill requests
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+PAGE_UNMAPPED = 0xFFFFFFFF
+
+# cache element types, shared vocabulary with the C ABI enum values
+DTYPE_BF16 = 0
+DTYPE_FP8_E4M3 = 1
+DTYPE_F32 = 2
+
+MLA_KV_NORM_DIM = 512
+MLA_ROPE_DIM = 64
+MLA_ROW = MLA_KV_NORM_DIM + MLA_ROPE_DIM
+
+
+def rng_for(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def bf16_bits(x) -> np.ndarray:
+    """Round fp32 values to bf16 (library cast) and return the uint16 bits."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def rope_table(rows: int, dim: int, base: float) -> np.ndarray:
+    """Precomputed freqs_cis table, fp32 ``[rows, dim]``.
+
+    Interleaved (cos, sin): entry ``[p, 2i] = cos(p * theta_i)`` and
+    ``[p, 2i+1] = sin(p * theta_i)`` with ``theta_i = base ** (-2i / dim)``,
+    evaluated in float64 and rounded once to float32.  Plain frequencies, no
+    long-context rescaling.
+    """
+    i = np.arange(dim // 2, dtype=np.float64)
+    theta = base ** (-2.0 * i / dim)
+    ang = np.arange(rows, dtype=np.float64)[:, None] * theta[None, :]
+    tab = np.empty((rows, dim), dtype=np.float64)
+    tab[:, 0::2] = np.cos(ang)
+    tab[:, 1::2] = np.sin(ang)
+    return tab.astype(np.float32)
+
+
+@dataclasses.dataclass
+class PagedCache:
+    """Host image of a paged cache plus its addressing metadata.
+
+    Dense layout ``[num_pages, kv_dim, num_layers, page_size, num_heads,
+    head_size]`` (kv index 0 is K).  Strides are in elements of ``dtype``.
+    """
+
+    data: np.ndarray  # uint16 (bf16) or uint8 (fp8), flat
+    dtype: int
+    scale: float
+    page_table: np.ndarray  # uint32 [B, max_pages_per_seq]
+    cache_lengths: np.ndarray  # uint32 [B] prior lengths
+    num_pages: int
+    kv_dim: int
+    num_layers: int
+    page_size: int
+    num_heads: int
+    head_size: int
+
+    @property
+    def max_pages_per_seq(self) -> int:
+        return int(self.page_table.shape[1])
+
+    @property
+    def strides(self):
+        s_head = self.head_size
+        s_token = self.num_heads * s_head
+        s_layer = self.page_size * s_token
+        s_kv = self.num_layers * s_layer
+        s_page = self.kv_dim * s_kv
+        return (s_page, s_kv, s_layer, s_token, s_head)
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == DTYPE_BF16 else 1
+
+    def view6(self) -> np.ndarray:
+        return self.data.reshape(self.num_pages, self.kv_dim, self.num_layers,
+                                 self.page_size, self.num_heads, self.head_size)
+
+
+def build_page_table(rng, total_lens, page_size, max_pages_per_seq, whole=False,
+                     spare_pages=0):
+    """Give request b the pages it needs from one seeded permutation.
+
+    Request b takes ``ceil(total_lens[b] / page_size)`` consecutive entries of
+    a random permutation of all pages (``max_pages_per_seq`` entries when
+    ``whole``); unused entries hold ``PAGE_UNMAPPED``.  ``spare_pages`` pages
+    are allocated but referenced by no request.
+    """
+    total_lens = np.asarray(total_lens, dtype=np.int64)
+    B = total_lens.shape[0]
+    if whole:
+        need = np.full(B, max_pages_per_seq, dtype=np.int64)
+    else:
+        need = (total_lens + page_size - 1) // page_size
+    assert np.all(need <= max_pages_per_seq)
+    num_pages = int(need.sum()) + spare_pages
+    perm = rng.permutation(num_pages).astype(np.uint32)
+    table = np.full((B, max_pages_per_seq), PAGE_UNMAPPED, dtype=np.uint32)
+    cur = 0
+    for b in range(B):
+        n = int(need[b])
+        table[b, :n] = perm[cur:cur + n]
+        cur += n
+    return table, num_pages
+
+
+def make_cache(rng, dtype, scale, page_table, cache_lengths, num_pages, kv_dim,
+               num_layers, page_size, num_heads, head_size) -> PagedCache:
+    """Cache filled with seeded random bytes, so every untouched byte is distinctive."""
+    n = num_pages * kv_dim * num_layers * page_size * num_heads * head_size
+    eb = 2 if dtype == DTYPE_BF16 else 1
+    raw = rng.integers(0, 256, size=n * eb, dtype=np.uint8)
+    data = raw.view(np.uint16) if eb == 2 else raw
+    return PagedCache(data=data, dtype=dtype, scale=float(scale),
+                      page_table=np.ascontiguousarray(page_table, dtype=np.uint32),
+                      cache_lengths=np.ascontiguousarray(cache_lengths, dtype=np.uint32),
+                      num_pages=num_pages, kv_dim=kv_dim, num_layers=num_layers,
+                      page_size=page_size, num_heads=num_heads, head_size=head_size)
+
+
+def offsets_from_lengths(new_lens) -> np.ndarray:
+    off = np.zeros(len(new_lens) + 1, dtype=np.uint32)
+    off[1:] = np.cumsum(np.asarray(new_lens, dtype=np.int64))
+    return off
+
+
+def new_slots(offsets, cache_lengths):
+    """(token, request, slot position) for every new token: pos = prior + index."""
+    out = []
+    for b in range(len(offsets) - 1):
+        for i in range(int(offsets[b + 1]) - int(offsets[b])):
+            out.append((int(offsets[b]) + i, b, int(cache_lengths[b]) + i))
+    return out
+
+
+def normal_bf16(rng, shape, mean=0.0, std=1.0, outlier_frac=0.0, outlier_mult=20.0):
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    if mean != 0.0:
+        x += np.float32(mean)
+    if outlier_frac > 0.0:
+        mask = rng.random(size=shape, dtype=np.float32) < outlier_frac
+        x[mask] *= np.float32(outlier_mult)
+    return bf16_bits(x)
+
+
+def fill_new_k_rows(rng, cache: PagedCache, offsets, layer_idx):
+    """Overwrite the K rows of new slots with N(0,1) bf16 (stand-in for a QKV GEMM)."""
+    v = cache.view6()
+    P = cache.page_size
+    for t, b, pos in new_slots(offsets, cache.cache_lengths):
+        page = int(cache.page_table[b, pos // P])
+        v[page, 0, layer_idx, pos % P, :, :] = normal_bf16(
+            rng, (cache.num_heads, cache.head_size))
+
+
+@dataclasses.dataclass
+class MLAWorkload:
+    name: str
+    q_rope: np.ndarray  # bf16 bits [T, H, 64]
+    kv_in: np.ndarray  # bf16 bits [T, 576]
+    offsets: np.ndarray  # uint32 [B+1]
+    freqs: np.ndarray  # f32 [rows, 64]
+    gamma: np.ndarray  # bf16 bits [512]
+    cache: PagedCache
+    layer_idx: int
+    epsilon: float
+
+    @property
+    def T(self):
+        return int(self.q_rope.shape[0])
+
+    @property
+    def H(self):
+        return int(self.q_rope.shape[1])
+
+    @property
+    def B(self):
+        return int(self.offsets.shape[0] - 1)
+
+
+def mla_workload(name, seed, new_lens, prior_lens, num_heads, page_size, max_seq_len,
+                 cache_dtype, num_layers=1, layer_idx=0, scale=1.0, outlier_frac=0.0,
+                 whole_pages=False, spare_pages=0, epsilon=1e-6) -> MLAWorkload:
+    rng = rng_for(seed)
+    new_lens = np.asarray(new_lens, dtype=np.int64)
+    prior_lens = np.asarray(prior_lens, dtype=np.int64)
+    offsets = offsets_from_lengths(new_lens)
+    T = int(offsets[-1])
+    max_pages = (max_seq_len + page_size - 1) // page_size
+    table, num_pages = build_page_table(rng, prior_lens + new_lens, page_size, max_pages,
+                                        whole=whole_pages, spare_pages=spare_pages)
+    cache = make_cache(rng, cache_dtype, scale, table, prior_lens, num_pages, 1,
+                       num_layers, page_size, 1, MLA_ROW)
+    q = normal_bf16(rng, (T, num_heads, MLA_ROPE_DIM), outlier_frac=outlier_frac)
+    kv = normal_bf16(rng, (T, MLA_ROW), outlier_frac=outlier_frac)
+    gamma = normal_bf16(rng, (MLA_KV_NORM_DIM,), mean=1.0, std=0.1)
+    freqs = rope_table(max_seq_len, MLA_ROPE_DIM, 10000.0)
+    return MLAWorkload(name, q, kv, offsets, freqs, gamma, cache, layer_idx, epsilon)
+
+
+def mla_tiny(cache_dtype=DTYPE_BF16, seed=1) -> MLAWorkload:
+    """2 requests, new [3,5], prior [0,7], 4 q heads, page 16, max_seq 64, 8 pages."""
+    return mla_workload("mla_tiny", seed, [3, 5], [0, 7], num_heads=4, page_size=16,
+                        max_seq_len=64, cache_dtype=cache_dtype, num_layers=2,
+                        layer_idx=1, whole_pages=True)
+
+
+def mla_decode(cache_dtype=DTYPE_FP8_E4M3, seed=2, num_requests=256) -> MLAWorkload:
+    """DeepSeek-V3 decode: 256 x 1 new token, prior U[1,8192], 128 q heads, page 128."""
+    rng = rng_for(seed + 1000)
+    prior = rng.integers(1, 8192, size=num_requests, endpoint=True)
+    return mla_workload("mla_decode", seed, np.ones(num_requests, np.int64), prior,
+                        num_heads=128, page_size=128, max_seq_len=16384,
+                        cache_dtype=cache_dtype)
+
+
+def mla_prefill(cache_dtype=DTYPE_BF16, seed=3, num_requests=16) -> MLAWorkload:
+    """Ragged prefill: 16 requests, new U[512,8192], prior 0, 1% outliers x20."""
+    rng = rng_for(seed + 1000)
+    new = rng.integers(512, 8192, size=num_requests, endpoint=True)
+    return mla_workload("mla_prefill", seed, new, np.zeros(num_requests, np.int64),
+                        num_heads=128, page_size=128, max_seq_len=16384,
+                        cache_dtype=cache_dtype, outlier_frac=0.01)
+
+
+@dataclasses.dataclass
+class GQAWorkload:
+    name: str
+    q_proj: np.ndarray  # bf16 bits [T, Hq, S]
+    offsets: np.ndarray
+    freqs: np.ndarray  # f32 [rows, S]
+    position_ids: Optional[np.ndarray]  # uint32 [T] or [3, T]
+    mrope_section: Optional[np.ndarray]  # uint32 [3]
+    interleaved: bool
+    cache: PagedCache
+    layer_idx: int
+
+    @property
+    def T(self):
+        return int(self.q_proj.shape[0])
+
+    @property
+    def B(self):
+        return int(self.offsets.shape[0] - 1)
+
+
+def gqa_workload(name, seed, new_lens, prior_lens, num_q_heads, num_kv_heads, head_size,
+                 page_size, freqs_rows, base, interleaved, position_mode=None,
+                 mrope_section=None, num_layers=2, layer_idx=1, spare_pages=0,
+                 pos_limit=None) -> GQAWorkload:
+    """position_mode: None (slot positions), "ids" ([T]) or "mrope" ([3, T])."""
+    rng = rng_for(seed)
+    new_lens = np.asarray(new_lens, dtype=np.int64)
+    prior_lens = np.asarray(prior_lens, dtype=np.int64)
+    offsets = offsets_from_lengths(new_lens)
+    T = int(offsets[-1])
+    total = prior_lens + new_lens
+    max_pages = int(max(1, (int(total.max()) + page_size - 1) // page_size)) if len(total) else 1
+    table, num_pages = build_page_table(rng, total, page_size, max_pages,
+                                        spare_pages=spare_pages)
+    cache = make_cache(rng, DTYPE_BF16, 1.0, table, prior_lens, num_pages, 2, num_layers,
+                       page_size, num_kv_heads, head_size)
+    fill_new_k_rows(rng, cache, offsets, layer_idx)
+    q = normal_bf16(rng, (T, num_q_heads, head_size))
+    lim = freqs_rows if pos_limit is None else pos_limit
+    pos_ids = None
+    sec = None
+    if position_mode == "ids":
+        pos_ids = rng.integers(0, lim, size=T, dtype=np.uint32)
+    elif position_mode == "mrope":
+        pos_ids = rng.integers(0, lim, size=(3, T), dtype=np.uint32)
+        sec = np.asarray(mrope_section, dtype=np.uint32)
+    freqs = rope_table(freqs_rows, head_size, base)
+    return GQAWorkload(name, q, offsets, freqs, pos_ids, sec, bool(interleaved), cache,
+                       layer_idx)
+
+
+def gqa_llama3(interleaved=True, position_mode=None, seed=4, num_requests=32) -> GQAWorkload:
+    """Llama-3-8B: 32 q / 8 kv heads, head 128, new U[1,2048], prior U[0,4096], page 128."""
+    rng = rng_for(seed + 1000)
+    new = rng.integers(1, 2048, size=num_requests, endpoint=True)
+    prior = rng.integers(0, 4096, size=num_requests, endpoint=True)
+    sec = (16, 24, 24) if position_mode == "mrope" else None
+    return gqa_workload("gqa_llama3", seed, new, prior, 32, 8, 128, 128, 8192, 500000.0,
+                        interleaved, position_mode=position_mode, mrope_section=sec)
+
+
+@dataclasses.dataclass
+class KNormWorkload:
+    name: str
+    offsets: np.ndarray
+    gamma: np.ndarray  # bf16 bits [G]
+    epsilon: float
+    weight_offset: float
+    multiply_before_cast: bool
+    cache: PagedCache
+    layer_idx: int
+
+    @property
+    def T(self):
+        return int(self.offsets[-1])
+
+    @property
+    def B(self):
+        return int(self.offsets.shape[0] - 1)
+
+
+def knorm_workload(name, seed, new_lens, prior_lens, num_kv_heads, head_size, page_size,
+                   gamma_len, weight_offset=0.0, multiply_before_cast=True, num_layers=2,
+                   layer_idx=1, spare_pages=0, epsilon=1e-6) -> KNormWorkload:
+    rng = rng_for(seed)
+    new_lens = np.asarray(new_lens, dtype=np.int64)
+    prior_lens = np.asarray(prior_lens, dtype=np.int64)
+    offsets = offsets_from_lengths(new_lens)
+    total = prior_lens + new_lens
+    max_pages = int(max(1, (int(total.max()) + page_size - 1) // page_size)) if len(total) else 1
+    table, num_pages = build_page_table(rng, total, page_size, max_pages,
+                                        spare_pages=spare_pages)
+    cache = make_cache(rng, DTYPE_BF16, 1.0, table, prior_lens, num_pages, 2, num_layers,
+                       page_size, num_kv_heads, head_size)
+    fill_new_k_rows(rng, cache, offsets, layer_idx)
+    gamma = normal_bf16(rng, (gamma_len,), mean=1.0, std=0.1)
+    return KNormWorkload(name, offsets, gamma, epsilon, float(weight_offset),
+                         bool(multiply_before_cast), cache, layer_idx)
+
+
+def knorm_paged(gamma_len=128, seed=5, num_requests=64) -> KNormWorkload:
+    """8 kv heads, head 128, page 64; each request decode (p=0.5) or prefill U[64,1024]."""
+    rng = rng_for(seed + 1000)
+    decode = rng.random(num_requests) < 0.5
+    pre = rng.integers(64, 1024, size=num_requests, endpoint=True)
+    new = np.where(decode, 1, pre)
+    prior = rng.integers(0, 2048, size=num_requests, endpoint=True)
+    return knorm_workload("knorm", seed, new, prior, 8, 128, 64, gamma_len)
+
+
+def algorithmic_bytes_mla(T, H, cache_dtype, distinct_positions=None):
+    """Bytes each launch must move: q in+out, kv row in, cache row out, freqs rows."""
+    c = 2 if cache_dtype == DTYPE_BF16 else 1
+    rows = T if distinct_positions is None else distinct_positions
+    return T * (2 * H * MLA_ROPE_DIM * 2 + MLA_ROW * 2 + MLA_ROW * c) + rows * MLA_ROPE_DIM * 4
+
+
+def algorithmic_bytes_gqa(T, Hq, Hk, S, distinct_rows):
+    return T * (2 * Hq * S * 2 + 2 * Hk * S * 2) + distinct_rows * S * 4
+
+
+def algorithmic_bytes_knorm(T, Hk, G):
+    return T * 2 * Hk * G * 2
+
+
+def ceil_div(a, b):
+    return (a + b - 1) // b
+
+
+__all__ = [n for n in dir() if not n.startswith("_") and n not in ("annotations", "math")]

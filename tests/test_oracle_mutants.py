@@ -1,0 +1,94 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped
+term, a wrong sign, index, operand or rounding rule), compiles it on the CPU
+and runs the pin tests against it: at least one pin must fail.  The real
+oracle is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import test_oracle_codecs as C
+import test_oracle_rmsnorm as N
+import test_oracle_rope as R
+import test_oracle_scatter as S
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("rope sign of the sine term", "*y0 = x0c - x1s;", "*y0 = x0c + x1s;"),
+    ("rope cos/sin swapped", "float x0c = x0 * c;", "float x0c = x0 * s;"),
+    ("rope second output", "*y1 = x0s + x1c;", "*y1 = x1c - x0s;"),
+    ("half-split partner", "*e1 = k + S / 2;", "*e1 = S - 1 - k;"),
+    ("mrope section boundary", "(k < sec[0] + sec[1]) ? 1u", "(k <= sec[0] + sec[1]) ? 1u"),
+    ("position ids ignored", "if (!sec) return position_ids[t];", "if (!sec) return pos_s;"),
+    ("rms eps dropped", "float d = sqrtf(mean + eps);", "float d = sqrtf(mean);"),
+    ("rms wrong count", "float mean = ss / (float)n;", "float mean = ss / (float)(n + 1);"),
+    ("rms square dropped", "float sq = x[j] * x[j];", "float sq = x[j];"),
+    ("gamma index shifted", "y[j] = xr * w[j];", "y[j] = xr * w[(j + 1) % n];"),
+    ("weight offset dropped", "+ weight_offset;", "+ 0.0f;"),
+    ("slot position off by one",
+     "uint64_t pos = (uint64_t)cache_lengths[b] + tok_i[t];",
+     "uint64_t pos = (uint64_t)cache_lengths[b] + tok_i[t] + 1;"),
+    ("row inside page", "uint64_t row = pos % L->page_size;",
+     "uint64_t row = (pos + 1) % L->page_size;"),
+    ("layer offset dropped", "(int64_t)layer * L->s_layer", "(int64_t)0 * L->s_layer"),
+    ("K rows taken from V", "uint16_t* k = cache + base + (int64_t)g * s_head;",
+     "uint16_t* k = cache + base + s_kv + (int64_t)g * s_head;"),
+    ("q head order", "uint16_t* yq = q_rope_out + ((int64_t)t * H + h) * ROPE;",
+     "uint16_t* yq = q_rope_out + ((int64_t)t * H + (H - 1 - h)) * ROPE;"),
+    ("bf16 truncates", "keep += 1u;", "keep += 0u;"),
+    ("e4m3 ties away from zero", "double r = nearbyint(n);", "double r = round(n);"),
+    ("e4m3 subnormal quantum", "q = ldexp(1.0, -9);", "q = ldexp(1.0, -10);"),
+    ("fp8 scale multiplies", "float z = y / scale;", "float z = y * scale;"),
+    ("offsets order unchecked", "if (offsets[b] > offsets[b + 1]) return 0;",
+     "if (0) return 0;"),
+    ("page id range unchecked", "if (page >= L->num_pages) {", "if (page == 0xffffffffu) {"),
+    ("position range unchecked", "if (pos >= freqs_rows) {", "if (pos > freqs_rows) {"),
+]
+
+PINS = [
+    (C.test_bf16_encode_matches_torch_random, {}),
+    (C.test_bf16_encode_ties_and_neighbours, {}),
+    (C.test_e4m3_decode_all_codes_match_torch, {}),
+    (C.test_e4m3_spec_points, {}),
+    (C.test_e4m3_encode_matches_torch_in_range, {}),
+    (R.test_rope_pairs_vs_complex_fp64, {}),
+    (R.test_mla_q_and_k_rope_vs_complex_fp64, {}),
+    (R.test_mla_position_zero_identity, {}),
+    (R.test_gqa_half_split_is_permuted_interleaved, {}),
+    (N.test_unit_weight_rms_closed_form, {"n": 512, "eps": 0.5}),
+    (N.test_rms_norm_vs_torch, {}),
+    (N.test_mla_latent_part_vs_torch, {}),
+    (N.test_knorm_subset_vs_torch, {"G": 16}),
+    (N.test_knorm_weight_offset_adds_to_gamma, {}),
+    (S.test_mla_tiny_writes_exactly_new_rows, {"dtype": 1}),
+    (S.test_gqa_rotates_only_new_k_rows, {}),
+    (S.test_knorm_touches_only_leading_cols_of_new_rows, {}),
+    (S.test_invalid_offsets_write_nothing, {}),
+    (S.test_position_past_table_skips_token, {}),
+    (S.test_unmapped_page_skips_cache_row_only, {}),
+    (S.test_fp8_scale_convention, {}),
+] + [(R.test_gqa_q_and_k_vs_complex_fp64, {"interleaved": i, "mode": m})
+     for i in (True, False) for m in (None, "ids", "mrope")]
+
+
+def test_real_oracle_passes_every_listed_pin(orc):
+    for fn, kw in PINS:
+        fn(orc, **kw)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, name
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    v = oracle.Variant(oracle.compile_source(str(path), str(tmp_path / "mutant.so")))
+    for fn, kw in PINS:
+        try:
+            fn(v, **kw)
+        except AssertionError:
+            return
+    pytest.fail("no pin caught the planted mistake: " + name)
