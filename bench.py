@@ -1,0 +1,453 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused per-token KV-cache write on GB300.
+
+Default workload: MLA decode, DeepSeek-V3 shape (256 requests x 1 new token,
+prior lengths U[1,8192], 128 q heads, 512 latent + 64 rope, page 128, FP8
+E4M3 cache out with scale 1.0).  A step is one call of
+``kvw_mla_rope_rmsnorm_quant`` over that batch: RoPE on q_rope and on the
+rope part, RMSNorm of the latent part, FP8 quantisation and the paged
+scatter.  Other workloads (``--workload``) measure the prefill, GQA and
+K-norm launches the same way.
+
+Timing: W warm-up steps, then K timed steps between a barrier and a device
+synchronize on both sides.  Each step's launch is bracketed by CUDA events on
+the stream it is launched on; before every step the L2 is flushed (512 MiB
+written, then 512 MiB read, so no input line is resident and no dirty line
+is left to write back) unless the inputs are larger than L2.  Values are
+whole-job throughput (tokens/s over all ranks, slowest rank's time).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_kv_cache_mla_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA fused RoPE/RMSNorm/FP8 KV-write tokens/s; achieved HBM GB/s vs peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    # name: (builder, kernel source, description)
+    "mla_decode": (lambda s: W.mla_decode(W.DTYPE_FP8_E4M3, seed=s), "mla_rope_rmsnorm_quant.cu",
+                   "MLA decode DeepSeek-V3: 256 req x 1 token, prior U[1,8192], H=128, "
+                   "512+64, page 128, FP8 E4M3 cache (scale 1.0)"),
+    "mla_decode_bf16": (lambda s: W.mla_decode(W.DTYPE_BF16, seed=s), "mla_rope_rmsnorm_quant.cu",
+                        "MLA decode DeepSeek-V3, bf16 cache"),
+    "mla_prefill_bf16": (lambda s: W.mla_prefill(W.DTYPE_BF16, seed=s + 1),
+                         "mla_rope_rmsnorm_quant.cu",
+                         "MLA ragged prefill: 16 req, new U[512,8192], H=128, 1% outliers x20, "
+                         "bf16 cache"),
+    "mla_prefill_fp8": (lambda s: W.mla_prefill(W.DTYPE_FP8_E4M3, seed=s + 1),
+                        "mla_rope_rmsnorm_quant.cu",
+                        "MLA ragged prefill: 16 req, new U[512,8192], H=128, 1% outliers x20, "
+                        "FP8 E4M3 cache"),
+    "gqa_interleaved": (lambda s: W.gqa_llama3(True, None, seed=s + 2), "qk_rope_paged_ragged.cu",
+                        "GQA Llama-3-8B Q/K RoPE, interleaved, slot positions"),
+    "gqa_half_ids": (lambda s: W.gqa_llama3(False, "ids", seed=s + 2), "qk_rope_paged_ragged.cu",
+                     "GQA Llama-3-8B Q/K RoPE, half-split, position_ids"),
+    "gqa_mrope": (lambda s: W.gqa_llama3(False, "mrope", seed=s + 2), "qk_rope_paged_ragged.cu",
+                  "GQA Llama-3-8B Q/K RoPE, half-split, mrope (16,24,24)"),
+    "knorm128": (lambda s: W.knorm_paged(128, seed=s + 3), "rms_norm_kv_cache_paged.cu",
+                 "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, G=128"),
+    "knorm64": (lambda s: W.knorm_paged(64, seed=s + 3), "rms_norm_kv_cache_paged.cu",
+                "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, "
+                "subset G=64"),
+}
+DEFAULT_SEED = {"mla": 2, "gqa": 2, "kno": 2}
+
+
+def kind(name):
+    return name[:3]
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def source_hash(kernel_file):
+    h = hashlib.sha256()
+    for f in (kernel_file, "kvw_device.cuh"):
+        h.update(open(os.path.join(ROOT, "gqa_kv_cache_mla_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "%s.md" % workload)
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hs = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not hs or hs.group(1) != source_hash(kernel_file):
+        return None
+    return float(m.group(1))
+
+
+def algorithmic_bytes(w, name):
+    k = kind(name)
+    if k == "mla":
+        c = w.cache
+        pos = np.concatenate([c.cache_lengths[b] + np.arange(w.offsets[b + 1] - w.offsets[b])
+                              for b in range(w.B)]) if w.T else np.zeros(0)
+        return W.algorithmic_bytes_mla(w.T, w.H, c.dtype, len(np.unique(pos)))
+    if k == "gqa":
+        c = w.cache
+        if w.position_ids is None:
+            rows = len(np.unique(np.concatenate(
+                [c.cache_lengths[b] + np.arange(w.offsets[b + 1] - w.offsets[b])
+                 for b in range(w.B)])))
+            return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, rows)
+        # mrope / ids: each distinct (row, pair-range) read counts; bound by distinct rows
+        rows = len(np.unique(w.position_ids))
+        per_row = c.head_size * 4
+        if w.mrope_section is not None:
+            # every position row supplies only its section's pairs
+            used = 0
+            for r, sec in enumerate(w.mrope_section):
+                used += len(np.unique(w.position_ids[r])) * int(sec) * 8
+            return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0) + used
+        return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0) + rows * per_row
+    c = w.cache
+    return W.algorithmic_bytes_knorm(w.T, c.num_heads, w.gamma.size)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, name, budget_s):
+    """The oracle, as it is, on the host cores, over whole batches of the
+    same workload until ``budget_s`` seconds of CPU time have elapsed."""
+    import oracle
+
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    if not oracle.has_openmp():
+        threads = 1
+    k = kind(name)
+    cache = w.cache.data.copy()  # written in place by every call (allocated once)
+    if k == "mla":
+        q_out = np.zeros_like(w.q_rope)
+        fn = lambda: oracle.mla_rope_rmsnorm_quant(w, q_rope_out=q_out, cache_data=cache,
+                                                   nthreads=threads)
+    elif k == "gqa":
+        out = np.zeros_like(w.q_proj)
+        fn = lambda: oracle.qk_rope_paged_ragged(w, output=out, cache_data=cache,
+                                                 nthreads=threads)
+    else:
+        fn = lambda: oracle.rms_norm_kv_cache_paged(w, cache_data=cache, nthreads=threads)
+    fn()  # warm: page in buffers
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    tps = n * w.T / el
+    return {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d whole batches of %d tokens (%s), %.1f s wall" % (n, w.T, name, el),
+            "gbs": algorithmic_bytes(w, name) * n / el / 1e9}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    name = args.workload
+    w = WORKLOADS[name][0](DEFAULT_SEED[kind(name)])
+    import oracle
+
+    oracle.build()
+    times = []
+    threads = None
+    # keep the whole run within about two minutes whatever K and W are
+    step_s = min(args.ref_step_s, 120.0 / (args.warmup + args.steps))
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, name, budget_s=step_s)
+        threads = cb["cores"]
+        if i >= args.warmup:
+            times.append(w.T / cb["value"])
+    ms = 1000.0 * statistics.mean(times)
+    value = w.T / (ms / 1000.0)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": name + ": " + WORKLOADS[name][2], "tokens": w.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": "each step: whole %d-token batches for %.2f s" %
+                                       (w.T, step_s)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from gqa_kv_cache_mla_gb300 import device as D
+    from gqa_kv_cache_mla_gb300 import kvw
+
+    name = args.workload
+    builder, kfile, desc = WORKLOADS[name]
+    # replicas: each rank writes its own independent batch (weak scaling)
+    w = builder(DEFAULT_SEED[kind(name)] + 100 * rank)
+    k = kind(name)
+    cls = {"mla": D.DeviceMLA, "gqa": D.DeviceGQA, "kno": D.DeviceKNorm}[k]
+    d = cls(w, device=dev, guard=False)
+    stream = torch.cuda.current_stream(dev)
+    run = lambda: d.run(stream=stream)
+    abytes = algorithmic_bytes(w, name)
+    footprint = abytes
+    flush = footprint < 2 * L2_BYTES
+    if flush:
+        fw = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        fr = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+
+    def l2_flush():
+        fw.fill_(1)
+        fr.sum()
+
+    for _ in range(args.warmup):
+        if flush:
+            l2_flush()
+        run()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush:
+            l2_flush()
+        ev[i][0].record(stream)
+        run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(per)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    tokens_all = w.T * world
+    value = tokens_all / (ms_max / 1000.0)
+    assert d.flags() == 0, "kernel reported data errors on the benchmark inputs"
+
+    # end to end through the public API: pinned host inputs -> device, launch,
+    # q/output and the error word back to the host, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(d, w, k, stream, dev, max(3, min(args.steps, 200)), args.warmup)
+        if world > 1:
+            t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["ms"] = float(t.item())
+        e2e = {"value": tokens_all / (e2e["ms"] / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+               "ms_per_step": e2e["ms"]}
+
+    peak, peak_src = measured_peak()
+    achieved = abytes / (ms / 1000.0) / 1e9
+    traffic = ncu_traffic(name, kfile)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": abytes,
+            "peak_source": peak_src, "kernel": kfile.replace(".cu", "")}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, name, budget_s=args.cpu_s)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC if k == "mla" else "%s tokens/s; achieved HBM GB/s vs peak" % name,
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; shapes and distributions of the benchmark configs)",
+        "config": {"workload": name + ": " + desc, "tokens_per_gpu": w.T,
+                   "l2": ("flushed before every step (512 MiB written, 512 MiB read)" if flush
+                          else "inputs larger than L2 (%.2f GB per step)" % (abytes / 1e9)),
+                   "io": "bf16 activations in, fp32 arithmetic, cache out %s" %
+                         ("e4m3" if getattr(w.cache, "dtype", 0) == W.DTYPE_FP8_E4M3 else "bf16"),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+        "clocks": clk,
+        "timing": {"ms_median": statistics.median(per), "ms_min": min(per),
+                   "wall_s_timed_region": wall, "kernel_source_sha256_16": source_hash(kfile)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure_e2e(d, w, k, stream, dev, steps, warmup):
+    """Host buffers in and out, copies inside the timed region."""
+    import torch
+
+    from gqa_kv_cache_mla_gb300 import device as D
+
+    def pinned(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+
+    if k == "mla":
+        ins = [d.q.tensor, d.kv.tensor, d.offsets.tensor, d.cache_lengths.tensor,
+               d.page_table.tensor]
+        outs = [d.q_out.tensor, d.err.tensor]
+    elif k == "gqa":
+        ins = [d.q.tensor, d.offsets.tensor, d.cache_lengths.tensor, d.page_table.tensor]
+        if d.pos is not None:
+            ins.append(d.pos.tensor)
+        outs = [d.out.tensor, d.err.tensor]
+    else:
+        ins = [d.offsets.tensor, d.cache_lengths.tensor, d.page_table.tensor]
+        outs = [d.err.tensor]
+    h_in = [pinned(t) for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def step():
+        for dst, src in zip(ins, h_in):
+            dst.copy_(src, non_blocking=True)
+        d.run(stream=stream)
+        for dst, src in zip(h_out, outs):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mla_decode")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-s", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--ref-step-s", type=float, default=2.0,
+                    help="seconds of oracle time per step of --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps is None:
+        args.steps = {"mla_decode": 4000, "mla_decode_bf16": 4000}.get(args.workload, 300)
+        if args.impl == "reference":
+            args.steps = 5
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

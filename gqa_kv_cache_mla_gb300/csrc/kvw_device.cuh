@@ -1,0 +1,141 @@
+// Device helpers shared by the three KV-cache write kernels (sm_103a).
+//
+// Everything here is memory plumbing and exact arithmetic building blocks:
+// 16-byte vector loads/stores with cache hints, exact bf16 widening, packed
+// bf16 / FP8 E4M3 conversion through the hardware cvt instructions, the
+// rotation of one pair, and the per-CTA ragged lookup (input_row_offsets ->
+// request -> slot position) that every kernel starts with.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kvw.h"
+
+namespace kvw {
+
+// ------------------------------------------------------------ memory access
+
+// Read-once stream (activations): evict-first in L1 and L2.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+// Write-once stream (outputs nobody rereads in this kernel).
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
+// Small tables reused by many CTAs (gamma, freqs rows, offsets): read-only path.
+__device__ __forceinline__ uint4 ld_table(const uint4* p) { return __ldg(p); }
+__device__ __forceinline__ float4 ld_table(const float4* p) { return __ldg(p); }
+
+// ------------------------------------------------------------ conversions
+
+// bf16 -> fp32 is exact: the bf16 pattern is the upper half of the fp32 one.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Two fp32 -> packed bf16x2, round to nearest even (one cvt.rn.bf16x2.f32).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// Two fp32 -> packed E4M3x2, round to nearest even, saturating to +-448
+// (one cvt.rn.satfinite.e4m3x2.f32).  Element `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8]) {
+    uint2 v;
+    v.x = pack_e4m3x2(f[0], f[1]) | (pack_e4m3x2(f[2], f[3]) << 16);
+    v.y = pack_e4m3x2(f[4], f[5]) | (pack_e4m3x2(f[6], f[7]) << 16);
+    return v;
+}
+
+// ------------------------------------------------------------ arithmetic
+
+// Rotation of one pair by (c, s) = (cos, sin): y0 = x0*c - x1*s,
+// y1 = x0*s + x1*c.  The _rn intrinsics keep every product rounded on its
+// own (never contracted into an FMA), so the result is the IEEE fp32 value
+// of that expression evaluated term by term.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0,
+                                          float& y1) {
+    y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
+    y1 = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
+}
+
+// 1 / sqrt(ss / n + eps) with correctly rounded divide and square root.
+__device__ __forceinline__ float rms_inv(float ss, float n, float eps) {
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), eps)));
+}
+
+__device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
+    if (err_flags) atomicOr(err_flags, bits);
+}
+
+// ------------------------------------------------------------ ragged lookup
+
+// Copy offsets[0..B] and cache_lengths[0..B-1] into shared memory and check
+// that the offsets start at 0, never decrease and end at T.  Every thread of
+// the CTA must call this; the result is uniform.
+__device__ __forceinline__ bool stage_ragged(const uint32_t* __restrict__ offsets,
+                                             const uint32_t* __restrict__ cache_lengths,
+                                             uint32_t B, uint32_t T, uint32_t* s_off,
+                                             uint32_t* s_clen) {
+    for (uint32_t i = threadIdx.x; i <= B; i += blockDim.x) {
+        s_off[i] = __ldg(offsets + i);
+        if (i < B) s_clen[i] = __ldg(cache_lengths + i);
+    }
+    __syncthreads();
+    int ok = 1;
+    for (uint32_t i = threadIdx.x; i < B; i += blockDim.x)
+        if (s_off[i] > s_off[i + 1]) ok = 0;
+    if (threadIdx.x == 0 && (s_off[0] != 0u || s_off[B] != T)) ok = 0;
+    return __syncthreads_and(ok) != 0;
+}
+
+// Request owning token t, for validated offsets (offsets[0] = 0 <= t <
+// offsets[B] = T): the largest b with offsets[b] <= t.  Binary search over
+// the staged copy.
+__device__ __forceinline__ uint32_t find_request(const uint32_t* s_off, uint32_t B, uint32_t t) {
+    uint32_t lo = 0, hi = B;  // s_off[lo] <= t < s_off[hi]
+    while (hi - lo > 1u) {
+        uint32_t mid = (lo + hi) >> 1;
+        if (s_off[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Element offset of the K row of slot `pos` of request b in `layer_off`, or
+// -1 when the slot maps to no valid page.
+__device__ __forceinline__ int64_t slot_row(const uint32_t* __restrict__ page_table,
+                                           uint32_t max_pages, uint32_t num_pages,
+                                           uint32_t page_size, int64_t s_page, int64_t s_token,
+                                           int64_t layer_off, uint32_t b, uint64_t pos) {
+    const uint64_t pidx = pos / page_size;
+    if (pidx >= max_pages) return -1;
+    const uint32_t page = __ldg(page_table + (uint64_t)b * max_pages + pidx);
+    if (page >= num_pages) return -1;
+    return (int64_t)page * s_page + layer_off + (int64_t)(pos % page_size) * s_token;
+}
+
+}  // namespace kvw

@@ -1,0 +1,313 @@
+// Fused MLA key-cache write: RoPE on q_rope and on the rope part of each
+// latent row, RMSNorm of the 512-wide latent part, quantisation to the cache
+// type and scatter through the page table.
+//
+// Operation: "mla_fused_rope_rmsnorm_quantization" (Modular MAX kernel API,
+// Mojo function page: description of the three fused operations; Args
+// q_rope_output, q_rope, input_row_offsets, freqs_cis, gamma, kv_collection,
+// layer_idx, epsilon; Parameters kv_input_fn) and the
+// fused_rope_rmsnorm_quantization_kernel entry of the "mla_graph" module page.
+//
+// GB300 design.  The launch is purely HBM-bound (about 0.5 flop per byte),
+// so the kernel is organised around keeping enough 16-byte loads in flight on
+// all 152 SMs:
+//   * CTAs [0, kv_blocks) own latent rows, one warp per token: lane l holds
+//     columns 8l..8l+7 and 256+8l..256+8l+7 of the latent part (lanes 0..7
+//     also one 8-wide slice of the rope part), a 5-step xor-shuffle gives the
+//     sum of squares, and the row leaves as one coalesced 576 B (FP8) or
+//     1152 B (bf16) store into its page slot.
+//   * the remaining CTAs stream q_rope as a flat array of 16-byte vectors,
+//     VPT vectors per thread, all loads issued before the ragged lookup so
+//     the lookup's latency hides under them.  A head row is 8 vectors and
+//     256 % 8 == 0, so a thread always works on the same 8 columns and needs
+//     one freqs slice per token.
+//   * every CTA stages input_row_offsets and cache_lengths in shared memory,
+//     validates them and binary-searches its tokens' requests there.
+// Both roles live in one launch so a decode step is one kernel.
+#include <cstdint>
+
+#include "kvw_device.cuh"
+
+namespace kvw {
+namespace {
+
+constexpr uint32_t kThreads = 256;
+constexpr uint32_t kRowsPerKvBlock = kThreads / 32;  // one warp per latent row
+constexpr uint32_t kNorm = 512, kRope = 64, kRow = kNorm + kRope;
+
+struct MlaArgs {
+    const uint4* q_in;   // bf16 [T, H, 64] as 16-byte vectors
+    uint4* q_out;        // bf16 [T, H, 64]
+    const uint16_t* kv_in;
+    int64_t kv_row_stride;  // elements
+    const uint32_t* offsets;
+    const uint32_t* cache_lengths;
+    const uint32_t* page_table;
+    const float* freqs;  // [freqs_rows, 64]
+    const uint4* gamma;  // bf16 [512]
+    void* cache;
+    uint32_t* err_flags;
+    int64_t s_page, s_token, layer_off;  // elements of the cache type
+    uint32_t q_vectors;                  // T * H * 8
+    uint32_t B, T, H, freqs_rows, max_pages, num_pages, page_size;
+    uint32_t kv_blocks;
+    float eps, scale;
+};
+
+template <bool FP8>
+__device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&y)[8], float scale) {
+    if constexpr (FP8) {
+        float z[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) z[i] = __fdiv_rn(y[i], scale);
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) = pack8_e4m3(z);
+    } else {
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(cache) + elem) = pack8_bf16(y);
+    }
+}
+
+// One warp per token: RMSNorm of the latent part, RoPE of the rope part,
+// quantise, write the 576-wide cache row.
+template <bool FP8>
+__device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
+    const bool active = t < a.T;
+    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
+    if (active) {
+        const uint4* row = reinterpret_cast<const uint4*>(a.kv_in + (int64_t)t * a.kv_row_stride);
+        x0 = ld_stream(row + lane);
+        x1 = ld_stream(row + 32 + lane);
+        if (lane < 8) xr = ld_stream(row + 64 + lane);
+        g0 = ld_table(a.gamma + lane);
+        g1 = ld_table(a.gamma + 32 + lane);
+    }
+    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    if (!active) return;
+    const uint32_t b = find_request(s_off, a.B, t);
+    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+    if (pos >= a.freqs_rows) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
+        return;
+    }
+    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                                  a.s_token, a.layer_off, b, pos);
+    if (base < 0) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
+        return;
+    }
+    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+    if (lane < 8) {
+        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
+        fa = ld_table(fr);
+        fb = ld_table(fr + 1);
+    }
+    // RMSNorm of the 512 latent values held 16 per lane.
+    float v0[8], v1[8], w0[8], w1[8];
+    unpack8(x0, v0);
+    unpack8(x1, v1);
+    unpack8(g0, w0);
+    unpack8(g1, w1);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(v0[i], v0[i]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(v1[i], v1[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const float r = rms_inv(ss, (float)kNorm, a.eps);
+    float y0[8], y1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        y0[i] = __fmul_rn(__fmul_rn(v0[i], r), w0[i]);
+        y1[i] = __fmul_rn(__fmul_rn(v1[i], r), w1[i]);
+    }
+    store8<FP8>(a.cache, base + lane * 8, y0, a.scale);
+    store8<FP8>(a.cache, base + 256 + lane * 8, y1, a.scale);
+    if (lane < 8) {  // rope part: 4 adjacent pairs per lane
+        float xv[8], yr[8];
+        unpack8(xr, xv);
+        rope_pair(xv[0], xv[1], fa.x, fa.y, yr[0], yr[1]);
+        rope_pair(xv[2], xv[3], fa.z, fa.w, yr[2], yr[3]);
+        rope_pair(xv[4], xv[5], fb.x, fb.y, yr[4], yr[5]);
+        rope_pair(xv[6], xv[7], fb.z, fb.w, yr[6], yr[7]);
+        store8<FP8>(a.cache, base + kNorm + lane * 8, yr, a.scale);
+    }
+}
+
+// q_rope streaming: VPT 16-byte vectors per thread.
+template <int VPT>
+__device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
+    __shared__ uint32_t s_pos[(kThreads * VPT) / 8 + 2];
+    const uint32_t qb = blockIdx.x - a.kv_blocks;
+    const uint32_t vbase = qb * (kThreads * VPT);
+    uint4 x[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) x[i] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const uint32_t v = vbase + threadIdx.x + i * kThreads;
+        if (v < a.q_vectors) x[i] = ld_stream(a.q_in + v);
+    }
+    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    const uint32_t vpt = a.H * 8u;  // vectors per token
+    const uint32_t t0 = vbase / vpt;
+    const uint32_t vlast = min(vbase + kThreads * VPT, a.q_vectors) - 1u;
+    const uint32_t ntok = vlast / vpt - t0 + 1u;
+    for (uint32_t k = threadIdx.x; k < ntok; k += kThreads) {
+        const uint32_t t = t0 + k;
+        const uint32_t b = find_request(s_off, a.B, t);
+        const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+        if (pos >= a.freqs_rows) {
+            s_pos[k] = 0xffffffffu;
+            flag(a.err_flags, KVW_ERR_POSITION);
+        } else {
+            s_pos[k] = (uint32_t)pos;
+        }
+    }
+    __syncthreads();
+    const uint32_t j = threadIdx.x & 7u;  // 8-column slice of the 64-wide head row
+    uint32_t cur_t = 0xffffffffu, p = 0xffffffffu;
+    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const uint32_t v = vbase + threadIdx.x + i * kThreads;
+        if (v >= a.q_vectors) break;
+        const uint32_t t = v / vpt;
+        if (t != cur_t) {
+            cur_t = t;
+            p = s_pos[t - t0];
+            if (p != 0xffffffffu) {
+                const float4* fr = reinterpret_cast<const float4*>(a.freqs + (uint64_t)p * kRope) + j * 2;
+                fa = ld_table(fr);
+                fb = ld_table(fr + 1);
+            }
+        }
+        if (p == 0xffffffffu) continue;
+        float xv[8], y[8];
+        unpack8(x[i], xv);
+        rope_pair(xv[0], xv[1], fa.x, fa.y, y[0], y[1]);
+        rope_pair(xv[2], xv[3], fa.z, fa.w, y[2], y[3]);
+        rope_pair(xv[4], xv[5], fb.x, fb.y, y[4], y[5]);
+        rope_pair(xv[6], xv[7], fb.z, fb.w, y[6], y[7]);
+        st_stream(a.q_out + v, pack8_bf16(y));
+    }
+}
+
+template <bool FP8, int VPT>
+__global__ void __launch_bounds__(kThreads) mla_rope_rmsnorm_quant_kernel(const MlaArgs a) {
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t* s_off = s_dyn;
+    uint32_t* s_clen = s_dyn + a.B + 1;
+    if (blockIdx.x < a.kv_blocks)
+        latent_rows<FP8>(a, s_off, s_clen);
+    else
+        q_rows<VPT>(a, s_off, s_clen);
+}
+
+template <bool FP8, int VPT>
+cudaError_t launch(const MlaArgs& a, uint32_t blocks, size_t smem, cudaStream_t stream) {
+    auto k = mla_rope_rmsnorm_quant_kernel<FP8, VPT>;
+    if (smem > 32 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    k<<<blocks, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace kvw
+
+extern "C" int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, const void* q_rope,
+                                          const uint32_t* input_row_offsets, uint32_t num_batches,
+                                          uint32_t tot_seq_len, uint32_t num_heads,
+                                          const void* freqs_cis, int32_t freq_dtype,
+                                          uint32_t freqs_rows, const void* gamma,
+                                          int32_t gamma_dtype, const void* kv_in,
+                                          int64_t kv_row_stride, const kvw_paged_cache_t* cache,
+                                          uint32_t layer_idx, float epsilon, uint32_t* err_flags,
+                                          cudaStream_t stream) {
+    using namespace kvw;
+    if (!cache) return KVW_EINVAL;
+    if (out_dtype != KVW_DTYPE_BF16 || freq_dtype != KVW_DTYPE_F32 || gamma_dtype != KVW_DTYPE_BF16)
+        return KVW_EUNSUPPORTED;
+    if (cache->dtype != KVW_DTYPE_BF16 && cache->dtype != KVW_DTYPE_FP8_E4M3) return KVW_EUNSUPPORTED;
+    if (cache->head_size != kRow || cache->num_heads != 1) return KVW_EUNSUPPORTED;
+    if (num_batches > KVW_MAX_BATCHES) return KVW_EUNSUPPORTED;
+    if (tot_seq_len == 0) return KVW_OK;
+    const bool fp8 = cache->dtype == KVW_DTYPE_FP8_E4M3;
+    const int64_t esz = fp8 ? 1 : 2;
+    if (!input_row_offsets || !freqs_cis || !gamma || !kv_in || !cache->data || !cache->page_table ||
+        !cache->cache_lengths)
+        return KVW_EINVAL;
+    if (num_heads > 0 && (!q_rope || !q_rope_out)) return KVW_EINVAL;
+    if (layer_idx >= cache->num_layers || cache->page_size == 0 || freqs_rows == 0 ||
+        cache->max_pages_per_seq == 0)
+        return KVW_EINVAL;
+    if (!(fp8 ? cache->scale > 0.0f : true) || !(epsilon >= 0.0f)) return KVW_EINVAL;
+    if (kv_row_stride < (int64_t)kRow || kv_row_stride % 8 != 0) return KVW_EINVAL;
+    if (!aligned16(freqs_cis) || !aligned16(gamma) || !aligned16(kv_in) || !aligned16(cache->data) ||
+        (num_heads > 0 && (!aligned16(q_rope) || !aligned16(q_rope_out))))
+        return KVW_EINVAL;
+    if ((cache->stride_page * esz) % 16 || (cache->stride_layer * esz) % 16 ||
+        (cache->stride_token * esz) % 16 || cache->stride_page <= 0 || cache->stride_token <= 0)
+        return KVW_EINVAL;
+    const uint64_t qvec = (uint64_t)tot_seq_len * num_heads * 8u;
+    if (qvec > 0xfffff000ull) return KVW_EUNSUPPORTED;
+
+    MlaArgs a;
+    a.q_in = static_cast<const uint4*>(q_rope);
+    a.q_out = static_cast<uint4*>(q_rope_out);
+    a.kv_in = static_cast<const uint16_t*>(kv_in);
+    a.kv_row_stride = kv_row_stride;
+    a.offsets = input_row_offsets;
+    a.cache_lengths = cache->cache_lengths;
+    a.page_table = cache->page_table;
+    a.freqs = static_cast<const float*>(freqs_cis);
+    a.gamma = static_cast<const uint4*>(gamma);
+    a.cache = cache->data;
+    a.err_flags = err_flags;
+    a.s_page = cache->stride_page;
+    a.s_token = cache->stride_token;
+    a.layer_off = (int64_t)layer_idx * cache->stride_layer;
+    a.q_vectors = (uint32_t)qvec;
+    a.B = num_batches;
+    a.T = tot_seq_len;
+    a.H = num_heads;
+    a.freqs_rows = freqs_rows;
+    a.max_pages = cache->max_pages_per_seq;
+    a.num_pages = cache->num_pages;
+    a.page_size = cache->page_size;
+    a.kv_blocks = (tot_seq_len + kRowsPerKvBlock - 1) / kRowsPerKvBlock;
+    a.eps = epsilon;
+    a.scale = cache->scale;
+
+    // Vectors per thread: small launches (decode) use 1 so that the q work
+    // spreads over every SM; large ones use 4 to keep 64 B per thread in flight.
+    int vpt = 4;
+    if (qvec < 152ull * 8 * kThreads * 4) vpt = (qvec < 152ull * 4 * kThreads * 2) ? 1 : 2;
+    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
+    const uint64_t blocks = a.kv_blocks + qblocks;
+    if (blocks > 0x7fffffffull) return KVW_EUNSUPPORTED;
+    const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
+    cudaError_t e;
+    if (fp8) {
+        e = vpt == 4 ? launch<true, 4>(a, (uint32_t)blocks, smem, stream)
+          : vpt == 2 ? launch<true, 2>(a, (uint32_t)blocks, smem, stream)
+                     : launch<true, 1>(a, (uint32_t)blocks, smem, stream);
+    } else {
+        e = vpt == 4 ? launch<false, 4>(a, (uint32_t)blocks, smem, stream)
+          : vpt == 2 ? launch<false, 2>(a, (uint32_t)blocks, smem, stream)
+                     : launch<false, 1>(a, (uint32_t)blocks, smem, stream);
+    }
+    return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
+}

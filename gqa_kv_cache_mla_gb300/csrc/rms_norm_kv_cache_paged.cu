@@ -1,0 +1,270 @@
+// In-place RMSNorm of the K-cache rows of new tokens.
+//
+// Operation: "rms_norm_kv_cache_ragged_paged" (Modular MAX kernel API, Mojo
+// function page: description of the ragged view built from total_seq_len and
+// input_row_offsets, the subset of leading columns given by the length of
+// gamma, weight_offset added to gamma, multiply_before_cast; parameter
+// per_head_norm).
+//
+// GB300 design.  A "row" is one (token, kv head) slice of gamma_len leading
+// columns (or the whole K row of a token when per_head_norm is off).  A team
+// of TL lanes (a power of two, 4..32) owns a row: lane l holds 16-byte
+// vectors l, l + TL, ... of it, sums its squares, and an xor-shuffle inside
+// the team finishes the reduction, so no shared memory or block barrier is
+// needed for the norm itself.  Each team handles RPT rows so every thread has
+// RPT x VPL 16-byte loads in flight.  The CTA first resolves the page slot of
+// the few tokens its rows belong to (ragged lookup in shared memory), then
+// reads, normalises and writes back in place.  Columns at or past gamma_len
+// are neither read into the sum nor written.
+#include <cstdint>
+
+#include "kvw_device.cuh"
+
+namespace kvw {
+namespace {
+
+constexpr uint32_t kThreads = 256;
+constexpr uint32_t kMaxCols = 2048;
+
+struct KnArgs {
+    uint16_t* cache;
+    const uint32_t* offsets;
+    const uint32_t* cache_lengths;
+    const uint32_t* page_table;
+    const uint16_t* gamma;
+    uint32_t* err_flags;
+    int64_t s_page, s_token, s_head, layer_off;
+    uint32_t B, T, S, G, max_pages, num_pages, page_size;
+    uint32_t rows_per_token;  // num_heads (per-head) or 1 (whole K row)
+    uint32_t per_head;
+    uint32_t tl_log2;         // team size = 1 << tl_log2
+    uint32_t nv;              // 16-byte vectors per row = ceil(G / 8)
+    uint32_t rows_per_block;
+    uint64_t rows;            // T * rows_per_token
+    float eps, wo;
+    int mbc;
+};
+
+template <int VPL, int RPT>
+__global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t* s_off = s_dyn;
+    uint32_t* s_clen = s_dyn + a.B + 1;
+    __shared__ int64_t s_base[kThreads * RPT / 4 + 2];
+
+    const uint32_t TL = 1u << a.tl_log2;
+    const uint32_t team = threadIdx.x >> a.tl_log2;
+    const uint32_t tl = threadIdx.x & (TL - 1u);
+    const uint32_t teams = kThreads >> a.tl_log2;
+    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows_per_block;
+    const uint32_t t_lo = (uint32_t)(r0 / a.rows_per_token);
+
+    // weights of this lane's columns (the same for every row)
+    float w[VPL][8];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        const uint32_t vec = tl + v * TL;
+        if (vec < a.nv) {
+            const uint32_t c = vec * 8u;
+            if (c + 8u <= a.G) {
+                float g[8];
+                unpack8(ld_table(reinterpret_cast<const uint4*>(a.gamma + c)), g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[v][e] = __fadd_rn(g[e], a.wo);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w[v][e] = (c + e < a.G) ? __fadd_rn(bf16_lo(a.gamma[c + e]), a.wo) : 0.0f;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[v][e] = 0.0f;
+        }
+    }
+
+    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    const uint64_t r_end = min(r0 + a.rows_per_block, a.rows);
+    const uint32_t t_hi = (uint32_t)((r_end - 1) / a.rows_per_token);
+    for (uint32_t k = threadIdx.x; k <= t_hi - t_lo; k += kThreads) {
+        const uint32_t t = t_lo + k;
+        const uint32_t b = find_request(s_off, a.B, t);
+        const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+        const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                                      a.s_token, a.layer_off, b, pos);
+        s_base[k] = base;
+        if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
+    }
+    __syncthreads();
+
+    // element offsets of this lane's vectors for each of its rows
+    int64_t addr[RPT][VPL];
+    bool live[RPT];
+    uint4 x[RPT][VPL];
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+        const uint64_t r = r0 + team + (uint64_t)q * teams;
+        live[q] = false;
+        int64_t base = -1;
+        uint32_t g = 0;
+        if (r < r_end) {
+            const uint32_t t = (uint32_t)(r / a.rows_per_token);
+            g = (uint32_t)(r % a.rows_per_token);
+            base = s_base[t - t_lo];
+            live[q] = base >= 0;
+        }
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            const uint32_t vec = tl + v * TL;
+            addr[q][v] = -1;
+            x[q][v] = make_uint4(0, 0, 0, 0);
+            if (live[q] && vec < a.nv) {
+                const uint32_t c = vec * 8u;  // column inside the normalised row
+                const int64_t off = a.per_head ? (int64_t)g * a.s_head + c
+                                               : (int64_t)(c / a.S) * a.s_head + (c % a.S);
+                addr[q][v] = base + off;
+                x[q][v] = *reinterpret_cast<const uint4*>(a.cache + addr[q][v]);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+        float xs[VPL][8];
+        float ss = 0.0f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            unpack8(x[q][v], xs[v]);
+            const uint32_t c = (tl + v * TL) * 8u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (c + e < a.G) ss = __fadd_rn(ss, __fmul_rn(xs[v][e], xs[v][e]));
+        }
+        for (uint32_t o = TL >> 1; o > 0; o >>= 1)
+            ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        if (!live[q]) continue;
+        const float r = rms_inv(ss, (float)a.G, a.eps);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            if (addr[q][v] < 0) continue;
+            const uint32_t c = (tl + v * TL) * 8u;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float xr = __fmul_rn(xs[v][e], r);
+                if (a.mbc) {
+                    y[e] = __fmul_rn(xr, w[v][e]);
+                } else {
+                    const float xr_c = __bfloat162float(__float2bfloat16_rn(xr));
+                    y[e] = __fmul_rn(xr_c, w[v][e]);
+                }
+            }
+            const uint4 out = pack8_bf16(y);
+            if (c + 8u <= a.G) {
+                *reinterpret_cast<uint4*>(a.cache + addr[q][v]) = out;
+            } else {  // ragged tail of the gamma-length slice: columns < G only
+                const uint32_t words[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (c + e < a.G)
+                        a.cache[addr[q][v] + e] = (uint16_t)(e & 1 ? words[e >> 1] >> 16 : words[e >> 1]);
+            }
+        }
+    }
+}
+
+template <int VPL, int RPT>
+cudaError_t launch(const KnArgs& a, size_t smem, cudaStream_t stream) {
+    auto k = rms_norm_kv_kernel<VPL, RPT>;
+    if (smem > 32 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const uint64_t blocks = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
+    k<<<(uint32_t)blocks, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace kvw
+
+extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const void* gamma,
+                                           uint32_t gamma_len, float epsilon, float weight_offset,
+                                           uint32_t layer_idx, uint32_t total_seq_len,
+                                           const uint32_t* input_row_offsets, uint32_t num_batches,
+                                           int multiply_before_cast, int per_head_norm,
+                                           uint32_t* err_flags, cudaStream_t stream) {
+    using namespace kvw;
+    if (!cache) return KVW_EINVAL;
+    if (cache->dtype != KVW_DTYPE_BF16) return KVW_EUNSUPPORTED;
+    const uint32_t S = cache->head_size;
+    if (S == 0 || S % 8 != 0) return KVW_EINVAL;
+    if (num_batches > KVW_MAX_BATCHES) return KVW_EUNSUPPORTED;
+    if (gamma_len == 0) return KVW_EINVAL;
+    if (per_head_norm ? gamma_len > S : (uint64_t)gamma_len != (uint64_t)S * cache->num_heads)
+        return KVW_EINVAL;
+    if (gamma_len > kMaxCols) return KVW_EUNSUPPORTED;
+    if (total_seq_len == 0 || cache->num_heads == 0) return KVW_OK;
+    if (!gamma || !input_row_offsets || !cache->data || !cache->page_table || !cache->cache_lengths)
+        return KVW_EINVAL;
+    if (layer_idx >= cache->num_layers || cache->page_size == 0 || cache->max_pages_per_seq == 0)
+        return KVW_EINVAL;
+    if (!(epsilon >= 0.0f)) return KVW_EINVAL;
+    if (!aligned16(gamma) || !aligned16(cache->data)) return KVW_EINVAL;
+    if ((cache->stride_page * 2) % 16 || (cache->stride_layer * 2) % 16 ||
+        (cache->stride_token * 2) % 16 || (cache->stride_head * 2) % 16 ||
+        cache->stride_page <= 0 || cache->stride_token <= 0)
+        return KVW_EINVAL;
+
+    KnArgs a;
+    a.cache = static_cast<uint16_t*>(cache->data);
+    a.offsets = input_row_offsets;
+    a.cache_lengths = cache->cache_lengths;
+    a.page_table = cache->page_table;
+    a.gamma = static_cast<const uint16_t*>(gamma);
+    a.err_flags = err_flags;
+    a.s_page = cache->stride_page;
+    a.s_token = cache->stride_token;
+    a.s_head = cache->stride_head;
+    a.layer_off = (int64_t)layer_idx * cache->stride_layer;
+    a.B = num_batches;
+    a.T = total_seq_len;
+    a.S = S;
+    a.G = gamma_len;
+    a.max_pages = cache->max_pages_per_seq;
+    a.num_pages = cache->num_pages;
+    a.page_size = cache->page_size;
+    a.per_head = per_head_norm ? 1u : 0u;
+    a.rows_per_token = per_head_norm ? cache->num_heads : 1u;
+    a.nv = (gamma_len + 7) / 8;
+    uint32_t tl = 4;
+    while (tl < a.nv && tl < 32) tl <<= 1;
+    a.tl_log2 = 0;
+    while ((1u << a.tl_log2) < tl) ++a.tl_log2;
+    const uint32_t vpl = (a.nv + tl - 1) / tl;
+    a.rows = (uint64_t)total_seq_len * a.rows_per_token;
+    a.eps = epsilon;
+    a.wo = weight_offset;
+    a.mbc = multiply_before_cast ? 1 : 0;
+    const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
+    const uint32_t teams = kThreads / tl;
+    cudaError_t e;
+    if (vpl <= 1) {
+        a.rows_per_block = teams * 4;
+        e = launch<1, 4>(a, smem, stream);
+    } else if (vpl <= 2) {
+        a.rows_per_block = teams * 2;
+        e = launch<2, 2>(a, smem, stream);
+    } else if (vpl <= 4) {
+        a.rows_per_block = teams;
+        e = launch<4, 1>(a, smem, stream);
+    } else {
+        a.rows_per_block = teams;
+        e = launch<8, 1>(a, smem, stream);
+    }
+    return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
+}

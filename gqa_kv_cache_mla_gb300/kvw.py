@@ -1,0 +1,189 @@
+"""Python binding of the kvw C ABI (``include/kvw.h``).
+
+Argument marshalling only: every function forwards device pointers, sizes
+and the current CUDA stream to the function of the same name in
+``libkvw.so`` and returns its status (raising :class:`KvwError` on a
+non-zero status unless ``check=False``).  All computation happens in the
+library's sm_103a kernels; there is no other code path.  The library is
+built in-tree by ``python -m gqa_kv_cache_mla_gb300.build``; importing this
+module without it raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkvw.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "kvw.h")
+
+KVW_OK, KVW_EINVAL, KVW_EUNSUPPORTED, KVW_ECUDA = 0, 1, 2, 3
+DTYPE_BF16, DTYPE_FP8_E4M3, DTYPE_F32 = 0, 1, 2
+ERR_PAGE, ERR_POSITION, ERR_OFFSETS = 1, 2, 4
+PAGE_UNMAPPED = 0xFFFFFFFF
+
+
+class KvwError(RuntimeError):
+    def __init__(self, status, where):
+        super().__init__("%s returned %d (%s)" % (where, status, status_string(status)))
+        self.status = status
+
+
+class PagedCacheT(ctypes.Structure):
+    """Mirror of ``kvw_paged_cache_t``."""
+
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("page_table", ctypes.c_void_p),
+        ("max_pages_per_seq", ctypes.c_uint32),
+        ("cache_lengths", ctypes.c_void_p),
+        ("num_pages", ctypes.c_uint32),
+        ("num_layers", ctypes.c_uint32),
+        ("page_size", ctypes.c_uint32),
+        ("num_heads", ctypes.c_uint32),
+        ("head_size", ctypes.c_uint32),
+        ("stride_page", ctypes.c_int64),
+        ("stride_kv", ctypes.c_int64),
+        ("stride_layer", ctypes.c_int64),
+        ("stride_token", ctypes.c_int64),
+        ("stride_head", ctypes.c_int64),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("kvw CUDA library missing (%s): build it with "
+                          "`python -m gqa_kv_cache_mla_gb300.build`" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, u32, i32, i64, f32 = (ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int64,
+                              ctypes.c_float)
+    pc = ctypes.POINTER(PagedCacheT)
+    L.kvw_mla_rope_rmsnorm_quant.restype = ctypes.c_int
+    L.kvw_mla_rope_rmsnorm_quant.argtypes = [vp, i32, vp, vp, u32, u32, u32, vp, i32, u32, vp, i32,
+                                             vp, i64, pc, u32, f32, vp, vp]
+    L.kvw_qk_rope_paged_ragged.restype = ctypes.c_int
+    L.kvw_qk_rope_paged_ragged.argtypes = [vp, vp, u32, u32, u32, pc, vp, u32, vp, ctypes.c_int,
+                                           vp, u32, vp, vp, vp]
+    L.kvw_rms_norm_kv_cache_paged.restype = ctypes.c_int
+    L.kvw_rms_norm_kv_cache_paged.argtypes = [pc, vp, u32, f32, f32, u32, u32, vp, u32,
+                                              ctypes.c_int, ctypes.c_int, vp, vp]
+    L.kvw_status_string.restype = ctypes.c_char_p
+    L.kvw_status_string.argtypes = [ctypes.c_int]
+    L.kvw_version.restype = ctypes.c_int
+    L.kvw_version.argtypes = []
+    return L
+
+
+lib = _load()
+
+
+def header_functions():
+    """Names of the functions ``include/kvw.h`` declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(kvw_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return lib.kvw_status_string(status).decode()
+
+
+def version() -> int:
+    return lib.kvw_version()
+
+
+def _ptr(x):
+    """Device address of a tensor (or an int address, or None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _done(status, name, check):
+    if check and status != KVW_OK:
+        raise KvwError(status, name)
+    return status
+
+
+def paged_cache(data, dtype, page_table, cache_lengths, num_pages, num_layers, page_size,
+                num_heads, head_size, strides, scale=1.0, max_pages_per_seq=None) -> PagedCacheT:
+    """Fill a ``kvw_paged_cache_t``; ``strides`` = (page, kv, layer, token, head) in elements."""
+    if max_pages_per_seq is None:
+        max_pages_per_seq = page_table.shape[-1]
+    s = PagedCacheT()
+    s.data = _ptr(data)
+    s.dtype = dtype
+    s.scale = scale
+    s.page_table = _ptr(page_table)
+    s.max_pages_per_seq = max_pages_per_seq
+    s.cache_lengths = _ptr(cache_lengths)
+    s.num_pages, s.num_layers, s.page_size = num_pages, num_layers, page_size
+    s.num_heads, s.head_size = num_heads, head_size
+    (s.stride_page, s.stride_kv, s.stride_layer, s.stride_token, s.stride_head) = strides
+    return s
+
+
+def kvw_mla_rope_rmsnorm_quant(q_rope_out, q_rope, input_row_offsets, freqs_cis, gamma, kv_in,
+                               cache: PagedCacheT, layer_idx: int, epsilon: float, err_flags=None,
+                               stream=None, *, num_batches=None, tot_seq_len=None,
+                               num_heads=None, freqs_rows=None, kv_row_stride=None,
+                               out_dtype=DTYPE_BF16, freq_dtype=DTYPE_F32,
+                               gamma_dtype=DTYPE_BF16, check=True) -> int:
+    B = input_row_offsets.shape[0] - 1 if num_batches is None else num_batches
+    T = q_rope.shape[0] if tot_seq_len is None else tot_seq_len
+    H = q_rope.shape[1] if num_heads is None else num_heads
+    rows = freqs_cis.shape[0] if freqs_rows is None else freqs_rows
+    stride = kv_in.stride(0) if kv_row_stride is None else kv_row_stride
+    st = lib.kvw_mla_rope_rmsnorm_quant(
+        _ptr(q_rope_out), out_dtype, _ptr(q_rope), _ptr(input_row_offsets), B, T, H,
+        _ptr(freqs_cis), freq_dtype, rows, _ptr(gamma), gamma_dtype, _ptr(kv_in), stride,
+        ctypes.byref(cache), layer_idx, epsilon, _ptr(err_flags), _stream(stream))
+    return _done(st, "kvw_mla_rope_rmsnorm_quant", check)
+
+
+def kvw_qk_rope_paged_ragged(q_proj, input_row_offsets, cache: PagedCacheT, freqs_cis,
+                             position_ids, interleaved: bool, mrope_section, layer_idx: int,
+                             output, err_flags=None, stream=None, *, num_batches=None,
+                             tot_seq_len=None, num_q_heads=None, freqs_rows=None,
+                             check=True) -> int:
+    B = input_row_offsets.shape[0] - 1 if num_batches is None else num_batches
+    T = q_proj.shape[0] if tot_seq_len is None else tot_seq_len
+    Hq = q_proj.shape[1] if num_q_heads is None else num_q_heads
+    rows = freqs_cis.shape[0] if freqs_rows is None else freqs_rows
+    sec = None
+    if mrope_section is not None:
+        sec = (ctypes.c_uint32 * 3)(*[int(v) for v in mrope_section])
+    st = lib.kvw_qk_rope_paged_ragged(
+        _ptr(q_proj), _ptr(input_row_offsets), B, T, Hq, ctypes.byref(cache), _ptr(freqs_cis),
+        rows, _ptr(position_ids), int(bool(interleaved)),
+        ctypes.cast(sec, ctypes.c_void_p) if sec is not None else None, layer_idx, _ptr(output),
+        _ptr(err_flags), _stream(stream))
+    return _done(st, "kvw_qk_rope_paged_ragged", check)
+
+
+def kvw_rms_norm_kv_cache_paged(cache: PagedCacheT, gamma, epsilon: float, weight_offset: float,
+                                layer_idx: int, total_seq_len: int, input_row_offsets,
+                                multiply_before_cast: bool = True, per_head_norm: bool = True,
+                                err_flags=None, stream=None, *, gamma_len=None,
+                                num_batches=None, check=True) -> int:
+    G = gamma.shape[0] if gamma_len is None else gamma_len
+    B = input_row_offsets.shape[0] - 1 if num_batches is None else num_batches
+    st = lib.kvw_rms_norm_kv_cache_paged(
+        ctypes.byref(cache), _ptr(gamma), G, epsilon, weight_offset, layer_idx, total_seq_len,
+        _ptr(input_row_offsets), B, int(bool(multiply_before_cast)), int(bool(per_head_norm)),
+        _ptr(err_flags), _stream(stream))
+    return _done(st, "kvw_rms_norm_kv_cache_paged", check)

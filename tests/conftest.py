@@ -19,3 +19,16 @@ def orc():
 
     oracle.build()
     return oracle
+
+
+def _build_library():
+    """Compile libkvw.so (host-side checks and the ABI tests load it) and the oracle."""
+    import shutil
+
+    if shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc"):
+        from gqa_kv_cache_mla_gb300 import build
+
+        build.build()
+
+
+_build_library()

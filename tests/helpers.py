@@ -28,16 +28,73 @@ def e4m3_ulp_diff(a, b):
     return np.abs(e4m3_ordinal(a) - e4m3_ordinal(b))
 
 
-def expected_slots(offsets, cache_lengths, page_table, page_size):
+def expected_slots(offsets, cache_lengths, page_table, page_size, num_pages=None):
     """Written (token, page, row-in-page, position) by the plain slot formula.
 
     Token i of request b goes to position cache_lengths[b] + i, which is row
-    position % page_size of page page_table[b][position // page_size].
+    position % page_size of page page_table[b][position // page_size].  With
+    ``num_pages``, slots that map to no valid page are left out.
     """
     out = []
     for b in range(len(offsets) - 1):
         for i in range(int(offsets[b + 1]) - int(offsets[b])):
             pos = int(cache_lengths[b]) + i
+            if pos // page_size >= page_table.shape[-1]:
+                continue
             page = int(page_table[b][pos // page_size])
+            if num_pages is not None and page >= num_pages:
+                continue
             out.append((int(offsets[b]) + i, page, pos % page_size, pos))
     return out
+
+
+def written_row_mask(cache, slots, layer_idx):
+    """Boolean [num_pages, num_layers, page_size] of K rows the call may write."""
+    m = np.zeros((cache.num_pages, cache.num_layers, cache.page_size), dtype=bool)
+    for _, page, row, _ in slots:
+        m[page, layer_idx, row] = True
+    return m
+
+
+def compare_cache(cache, gpu, ref, slots, layer_idx, fp8, max_ulp_frac=None, cols=None):
+    """GPU cache vs oracle cache.
+
+    Elements outside the rows the call writes (and, with ``cols``, columns at
+    or past ``cols``) must be bit-identical; inside, bf16 may differ by 1 ulp
+    and FP8 by 1 ulp on at most ``max_ulp_frac`` of the written elements.
+    Returns the number of differing elements.
+    """
+    gpu = gpu.reshape(-1)
+    ref = ref.reshape(-1)
+    diff = np.flatnonzero(gpu != ref)
+    if diff.size == 0:
+        return 0
+    shape = (cache.num_pages, cache.kv_dim, cache.num_layers, cache.page_size, cache.num_heads,
+             cache.head_size)
+    page, kv, layer, row, head, col = np.unravel_index(diff, shape)
+    mask = written_row_mask(cache, slots, layer_idx)
+    inside = (kv == 0) & mask[page, layer, row]
+    if cols is not None:
+        inside &= col < cols
+    assert inside.all(), "bytes changed outside the written rows: %d" % int((~inside).sum())
+    if fp8:
+        u = e4m3_ulp_diff(gpu[diff], ref[diff])
+        assert u.max() <= 1, "fp8 difference above 1 ulp: %d" % int(u.max())
+        n_written = len(slots) * cache.num_heads * (cols or cache.head_size)
+        frac = diff.size / max(1, n_written)
+        assert frac <= (max_ulp_frac if max_ulp_frac is not None else 1e-3), frac
+    else:
+        u = bf16_ulp_diff(gpu[diff], ref[diff])
+        assert u.max() <= 1, "bf16 difference above 1 ulp: %d" % int(u.max())
+    return int(diff.size)
+
+
+def compare_bf16(gpu, ref):
+    """bf16 arrays equal within 1 ulp; returns the number of 1-ulp differences."""
+    gpu = np.asarray(gpu).reshape(-1)
+    ref = np.asarray(ref).reshape(-1)
+    diff = np.flatnonzero(gpu != ref)
+    if diff.size:
+        u = bf16_ulp_diff(gpu[diff], ref[diff])
+        assert u.max() <= 1, "bf16 difference above 1 ulp: %d" % int(u.max())
+    return int(diff.size)

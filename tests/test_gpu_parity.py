@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every case builds a seeded workload, runs the oracle on the host and the
+kernel on the device on the same bytes, and compares element by element:
+  * bytes outside the rows a call may write: bit-identical (guard bytes
+    around every device buffer included);
+  * bf16 outputs: at most 1 bf16 ulp from the oracle's fp32 result rounded
+    to bf16;
+  * FP8 E4M3 cache values: at most 1 E4M3 ulp on at most 0.1% of the written
+    elements (scale convention: stored = satfinite_rne(y / scale));
+  * error flags: equal.
+The five benchmark workloads run at full size in the launch configuration
+the benchmark uses; small cases cover edges.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from gqa_kv_cache_mla_gb300 import workloads as W
+from helpers import compare_bf16, compare_cache, expected_slots
+
+pytestmark = pytest.mark.gpu
+
+NTHREADS = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gqa_kv_cache_mla_gb300 import device
+
+    return device
+
+
+def run_mla(orc, dev, w, **kw):
+    d = dev.DeviceMLA(w)
+    d.run()
+    import torch
+
+    torch.cuda.synchronize()
+    q_ref, c_ref, f_ref = orc.mla_rope_rmsnorm_quant(w, q_rope_out=d.q_out_init.copy(),
+                                                     nthreads=NTHREADS)
+    assert d.guards_intact()
+    assert d.flags() == f_ref
+    c = w.cache
+    nq = compare_bf16(d.q_out.host(), q_ref)
+    slots = [] if f_ref & 4 else expected_slots(w.offsets, c.cache_lengths, c.page_table,
+                                                c.page_size, c.num_pages)
+    nc = compare_cache(c, d.cache.host(), c_ref, slots, w.layer_idx,
+                       fp8=c.dtype == W.DTYPE_FP8_E4M3)
+    return d, nq, nc
+
+
+# ------------------------------------------------------------------ MLA
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_FP8_E4M3])
+def test_mla_tiny(orc, dev, dtype):
+    run_mla(orc, dev, W.mla_tiny(cache_dtype=dtype))
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_FP8_E4M3, W.DTYPE_BF16])
+def test_mla_decode_full(orc, dev, dtype):
+    run_mla(orc, dev, W.mla_decode(cache_dtype=dtype))
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_FP8_E4M3])
+def test_mla_prefill_full(orc, dev, dtype):
+    run_mla(orc, dev, W.mla_prefill(cache_dtype=dtype))
+
+
+@pytest.mark.parametrize("H", [0, 1, 3, 16, 33])
+def test_mla_head_counts_and_ragged_tail(orc, dev, H):
+    w = W.mla_workload("h", 200 + H, [1, 0, 37, 5, 130], [3, 9, 0, 250, 17], num_heads=H,
+                       page_size=16, max_seq_len=512, cache_dtype=W.DTYPE_FP8_E4M3,
+                       num_layers=3, layer_idx=2, spare_pages=3)
+    run_mla(orc, dev, w)
+
+
+def test_mla_strided_kv_rows(orc, dev):
+    w = W.mla_workload("s", 211, [7, 9], [0, 100], num_heads=8, page_size=32, max_seq_len=256,
+                       cache_dtype=W.DTYPE_BF16)
+    rng = np.random.default_rng(5)
+    wide = rng.integers(0, 2**16, size=(w.T, 640), dtype=np.uint16)
+    wide[:, 64:640] = w.kv_in  # the 576-wide rows sit at column 64 of a 640-wide buffer
+    d = dev.DeviceMLA(w)
+    import torch
+
+    buf = torch.from_numpy(wide.view(np.int16)).to("cuda")
+    from gqa_kv_cache_mla_gb300 import kvw
+
+    kvw.kvw_mla_rope_rmsnorm_quant(d.q_out.tensor, d.q.tensor, d.offsets.tensor, d.freqs.tensor,
+                                   d.gamma.tensor, buf[:, 64:], d.desc, w.layer_idx, w.epsilon,
+                                   d.err.tensor, kv_row_stride=640)
+    torch.cuda.synchronize()
+    q_ref, c_ref, f = orc.mla_rope_rmsnorm_quant(w, q_rope_out=d.q_out_init.copy())
+    c = w.cache
+    compare_bf16(d.q_out.host(), q_ref)
+    compare_cache(c, d.cache.host(), c_ref,
+                  expected_slots(w.offsets, c.cache_lengths, c.page_table, c.page_size),
+                  w.layer_idx, fp8=False)
+
+
+def test_mla_many_requests_and_page_size_one(orc, dev):
+    rng = np.random.default_rng(7)
+    B = 3000
+    new = rng.integers(0, 3, B)
+    prior = rng.integers(0, 60, B)
+    w = W.mla_workload("m", 212, new, prior, num_heads=2, page_size=1, max_seq_len=64,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    run_mla(orc, dev, w)
+
+
+def test_mla_error_flags(orc, dev):
+    # position past the table
+    w = W.mla_workload("p", 91, [2, 5], [0, 60], num_heads=2, page_size=16, max_seq_len=80,
+                       cache_dtype=W.DTYPE_BF16)
+    w.freqs = w.freqs[:64].copy()
+    d, _, _ = run_mla(orc, dev, w)
+    assert d.flags() == 2
+    # unmapped page
+    w = W.mla_tiny()
+    w.cache.page_table[1, 0] = W.PAGE_UNMAPPED
+    d, _, _ = run_mla(orc, dev, w)
+    assert d.flags() == 1
+    # bad offsets: nothing written
+    for bad in ([1, 3, 8], [0, 5, 3, 8], [0, 3, 7]):
+        w = W.mla_tiny()
+        w.offsets = np.array(bad, np.uint32)
+        d = dev.DeviceMLA(w)
+        d.run(tot_seq_len=8)
+        import torch
+
+        torch.cuda.synchronize()
+        assert d.flags() == 4
+        assert np.array_equal(d.cache.host(), w.cache.data)
+        assert np.array_equal(d.q_out.host(), d.q_out_init)
+
+
+def test_mla_empty_and_repeat(orc, dev):
+    import torch
+
+    w = W.mla_workload("e", 93, [0, 0], [3, 0], num_heads=2, page_size=16, max_seq_len=32,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    d = dev.DeviceMLA(w)
+    d.run()
+    torch.cuda.synchronize()
+    assert d.flags() == 0 and np.array_equal(d.cache.host(), w.cache.data)
+    # two identical calls give identical bytes
+    w = W.mla_tiny(cache_dtype=W.DTYPE_FP8_E4M3)
+    d = dev.DeviceMLA(w)
+    d.run()
+    torch.cuda.synchronize()
+    a = (d.q_out.host().copy(), d.cache.host().copy())
+    d.cache.reset(w.cache.data)
+    s = torch.cuda.Stream()
+    d.run(stream=s)
+    s.synchronize()
+    assert np.array_equal(a[0], d.q_out.host()) and np.array_equal(a[1], d.cache.host())
+
+
+# ------------------------------------------------------------------ GQA
+
+def run_gqa(orc, dev, w, alias=False):
+    import torch
+
+    d = dev.DeviceGQA(w, alias_output=alias)
+    d.run()
+    torch.cuda.synchronize()
+    out0 = w.q_proj.copy() if alias else d.out_init.copy()
+    if alias:
+        w2 = W.GQAWorkload(**{**w.__dict__})
+        w2.q_proj = out0
+        out_ref, c_ref, f_ref = orc.qk_rope_paged_ragged(w2, output=out0, nthreads=NTHREADS)
+    else:
+        out_ref, c_ref, f_ref = orc.qk_rope_paged_ragged(w, output=out0, nthreads=NTHREADS)
+    assert d.guards_intact()
+    assert d.flags() == f_ref
+    c = w.cache
+    compare_bf16(d.out.host(), out_ref)
+    slots = [] if f_ref & 4 else expected_slots(w.offsets, c.cache_lengths, c.page_table,
+                                                c.page_size, c.num_pages)
+    compare_cache(c, d.cache.host(), c_ref, slots, w.layer_idx, fp8=False)
+    return d
+
+
+@pytest.mark.parametrize("interleaved", [True, False])
+@pytest.mark.parametrize("mode", [None, "ids", "mrope"])
+def test_gqa_llama3_full(orc, dev, interleaved, mode):
+    run_gqa(orc, dev, W.gqa_llama3(interleaved=interleaved, position_mode=mode))
+
+
+@pytest.mark.parametrize("S,Hq,Hk,sec", [(64, 8, 2, (5, 20, 7)), (256, 4, 1, (40, 44, 44)),
+                                         (16, 3, 1, (1, 3, 4)), (128, 64, 8, (16, 24, 24))])
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_gqa_shapes_and_odd_sections(orc, dev, S, Hq, Hk, sec, interleaved):
+    w = W.gqa_workload("s", 300 + S, [3, 0, 17, 1, 40], [0, 5, 100, 31, 7], Hq, Hk, S,
+                       page_size=16, freqs_rows=256, base=10000.0, interleaved=interleaved,
+                       position_mode="mrope", mrope_section=sec, spare_pages=2)
+    run_gqa(orc, dev, w)
+    w = W.gqa_workload("s", 400 + S, [3, 0, 17, 1, 40], [0, 5, 100, 31, 7], Hq, Hk, S,
+                       page_size=16, freqs_rows=256, base=10000.0, interleaved=interleaved)
+    run_gqa(orc, dev, w)
+
+
+def test_gqa_output_aliases_input(orc, dev):
+    w = W.gqa_workload("a", 501, [4, 9, 1], [3, 0, 20], 8, 2, 128, page_size=16,
+                       freqs_rows=64, base=500000.0, interleaved=False, position_mode="ids")
+    run_gqa(orc, dev, w, alias=True)
+
+
+def test_gqa_error_flags(orc, dev):
+    w = W.gqa_workload("g", 72, [3, 5], [0, 7], 2, 2, 16, page_size=16, freqs_rows=64,
+                       base=10000.0, interleaved=True, position_mode="ids")
+    w.position_ids[4] = 64
+    w.cache.page_table[0, 0] = W.PAGE_UNMAPPED
+    d = run_gqa(orc, dev, w)
+    assert d.flags() == 3
+
+
+# ------------------------------------------------------------------ K norm
+
+def run_knorm(orc, dev, w, per_head_norm=True):
+    import torch
+
+    d = dev.DeviceKNorm(w)
+    d.run(per_head_norm=per_head_norm)
+    torch.cuda.synchronize()
+    c_ref, f_ref = orc.rms_norm_kv_cache_paged(w, per_head_norm=per_head_norm, nthreads=NTHREADS)
+    assert d.guards_intact()
+    assert d.flags() == f_ref
+    c = w.cache
+    slots = [] if f_ref & 4 else expected_slots(w.offsets, c.cache_lengths, c.page_table,
+                                                c.page_size, c.num_pages)
+    compare_cache(c, d.cache.host(), c_ref, slots, w.layer_idx, fp8=False,
+                  cols=w.gamma.size if per_head_norm else None)
+    return d
+
+
+@pytest.mark.parametrize("G", [128, 64])
+def test_knorm_full(orc, dev, G):
+    run_knorm(orc, dev, W.knorm_paged(gamma_len=G))
+
+
+@pytest.mark.parametrize("G,S", [(100, 128), (8, 8), (24, 32), (256, 256), (512, 512),
+                                 (1000, 1024)])
+def test_knorm_widths(orc, dev, G, S):
+    w = W.knorm_workload("w", 600 + G, [2, 0, 30, 1], [5, 0, 13, 61], 3, S, page_size=8,
+                         gamma_len=G, spare_pages=2)
+    run_knorm(orc, dev, w)
+
+
+def test_knorm_variants(orc, dev):
+    w = W.knorm_workload("v", 611, [2, 9, 1], [5, 0, 13], 4, 64, page_size=16, gamma_len=64,
+                         weight_offset=0.5, multiply_before_cast=False)
+    run_knorm(orc, dev, w)
+    w = W.knorm_workload("v", 612, [2, 9, 1], [5, 0, 13], 4, 64, page_size=16, gamma_len=256)
+    run_knorm(orc, dev, w, per_head_norm=False)
+
+
+def test_knorm_error_flags(orc, dev):
+    w = W.knorm_workload("f", 613, [2, 3], [5, 20], 2, 32, page_size=8, gamma_len=32)
+    w.cache.page_table[1, 2] = W.PAGE_UNMAPPED  # positions 16..23 of request 1
+    d = run_knorm(orc, dev, w)
+    assert d.flags() == 1
