@@ -43,33 +43,7 @@ METRIC = "MLA fused RoPE/RMSNorm/FP8 KV-write tokens/s; achieved HBM GB/s vs pea
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 
-WORKLOADS = {
-    # name: (builder, kernel source, description)
-    "mla_decode": (lambda s: W.mla_decode(W.DTYPE_FP8_E4M3, seed=s), "mla_rope_rmsnorm_quant.cu",
-                   "MLA decode DeepSeek-V3: 256 req x 1 token, prior U[1,8192], H=128, "
-                   "512+64, page 128, FP8 E4M3 cache (scale 1.0)"),
-    "mla_decode_bf16": (lambda s: W.mla_decode(W.DTYPE_BF16, seed=s), "mla_rope_rmsnorm_quant.cu",
-                        "MLA decode DeepSeek-V3, bf16 cache"),
-    "mla_prefill_bf16": (lambda s: W.mla_prefill(W.DTYPE_BF16, seed=s + 1),
-                         "mla_rope_rmsnorm_quant.cu",
-                         "MLA ragged prefill: 16 req, new U[512,8192], H=128, 1% outliers x20, "
-                         "bf16 cache"),
-    "mla_prefill_fp8": (lambda s: W.mla_prefill(W.DTYPE_FP8_E4M3, seed=s + 1),
-                        "mla_rope_rmsnorm_quant.cu",
-                        "MLA ragged prefill: 16 req, new U[512,8192], H=128, 1% outliers x20, "
-                        "FP8 E4M3 cache"),
-    "gqa_interleaved": (lambda s: W.gqa_llama3(True, None, seed=s + 2), "qk_rope_paged_ragged.cu",
-                        "GQA Llama-3-8B Q/K RoPE, interleaved, slot positions"),
-    "gqa_half_ids": (lambda s: W.gqa_llama3(False, "ids", seed=s + 2), "qk_rope_paged_ragged.cu",
-                     "GQA Llama-3-8B Q/K RoPE, half-split, position_ids"),
-    "gqa_mrope": (lambda s: W.gqa_llama3(False, "mrope", seed=s + 2), "qk_rope_paged_ragged.cu",
-                  "GQA Llama-3-8B Q/K RoPE, half-split, mrope (16,24,24)"),
-    "knorm128": (lambda s: W.knorm_paged(128, seed=s + 3), "rms_norm_kv_cache_paged.cu",
-                 "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, G=128"),
-    "knorm64": (lambda s: W.knorm_paged(64, seed=s + 3), "rms_norm_kv_cache_paged.cu",
-                "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, "
-                "subset G=64"),
-}
+WORKLOADS = W.REGISTRY
 DEFAULT_SEED = {"mla": 2, "gqa": 2, "kno": 2}
 
 

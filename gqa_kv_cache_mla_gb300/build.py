@@ -23,7 +23,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvw.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-              "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+              "--expt-relaxed-constexpr", "-I", INCLUDE]
 
 
 def nvcc() -> str:
@@ -45,15 +45,14 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build_lib(csrc: str, out: str, objdir: str, verbose: bool = False, extra=()) -> str:
+    """Compile every ``*.cu`` of ``csrc`` and link them into ``out``."""
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [cc, *ARCH, *NVCC_FLAGS, "-I", csrc, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
@@ -61,15 +60,23 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
             print(r.stdout + r.stderr, file=sys.stderr)
         return obj
 
+    srcs = sorted(glob.glob(os.path.join(csrc, "*.cu")))
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp%d" % os.getpid()
+        objs = list(ex.map(compile_one, srcs))
+    tmp = out + ".tmp%d" % os.getpid()
     r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False, verbose: bool = False, extra=()) -> str:
+    """Build ``libkvw.so`` next to this file if any source is newer."""
+    if not force and not _stale():
+        return LIB
+    return build_lib(CSRC, LIB, BUILD, verbose=verbose, extra=extra)
 
 
 if __name__ == "__main__":

@@ -91,23 +91,74 @@ __device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
 
 // ------------------------------------------------------------ ragged lookup
 
-// Copy offsets[0..B] and cache_lengths[0..B-1] into shared memory and check
-// that the offsets start at 0, never decrease and end at T.  Every thread of
-// the CTA must call this; the result is uniform.
+// Ragged metadata staging, split in two so a kernel can put the table loads
+// at the head of its memory traffic:
+//   RaggedLoads r; r.issue(...)   loads offsets[i], offsets[i+1] and
+//                                 cache_lengths[i] for the first kRegRounds
+//                                 slices of the table into registers;
+//   ...                           the kernel issues its bulk loads here;
+//   r.commit(...)                 writes the shared copy (looping over any
+//                                 remainder), checks that the offsets start at
+//                                 0, never decrease and end at T, and returns
+//                                 that verdict through one barrier.
+// Every thread of the CTA must call both; the verdict is uniform.
+struct RaggedLoads {
+    static constexpr int kRegRounds = 2;
+    uint32_t off[kRegRounds], nxt[kRegRounds], clen[kRegRounds];
+
+    __device__ __forceinline__ void issue(const uint32_t* __restrict__ offsets,
+                                          const uint32_t* __restrict__ cache_lengths,
+                                          uint32_t B) {
+#pragma unroll
+        for (int k = 0; k < kRegRounds; ++k) {
+            const uint32_t i = threadIdx.x + k * blockDim.x;
+            off[k] = nxt[k] = clen[k] = 0;
+            if (i <= B) off[k] = __ldg(offsets + i);
+            if (i < B) {
+                nxt[k] = __ldg(offsets + i + 1);
+                clen[k] = __ldg(cache_lengths + i);
+            }
+        }
+    }
+
+    __device__ __forceinline__ bool commit(const uint32_t* __restrict__ offsets,
+                                           const uint32_t* __restrict__ cache_lengths,
+                                           uint32_t B, uint32_t T, uint32_t* s_off,
+                                           uint32_t* s_clen) const {
+        int ok = 1;
+#pragma unroll
+        for (int k = 0; k < kRegRounds; ++k) {
+            const uint32_t i = threadIdx.x + k * blockDim.x;
+            if (i <= B) {
+                s_off[i] = off[k];
+                if ((i == 0 && off[k] != 0u) || (i == B && off[k] != T)) ok = 0;
+            }
+            if (i < B) {
+                s_clen[i] = clen[k];
+                if (off[k] > nxt[k]) ok = 0;
+            }
+        }
+        for (uint32_t i = threadIdx.x + kRegRounds * blockDim.x; i <= B; i += blockDim.x) {
+            const uint32_t o = __ldg(offsets + i);
+            s_off[i] = o;
+            if (i < B) {
+                s_clen[i] = __ldg(cache_lengths + i);
+                if (o > __ldg(offsets + i + 1)) ok = 0;
+            }
+            if (i == B && o != T) ok = 0;
+        }
+        return __syncthreads_and(ok) != 0;
+    }
+};
+
+// Both halves at once, for kernels with nothing to overlap.
 __device__ __forceinline__ bool stage_ragged(const uint32_t* __restrict__ offsets,
                                              const uint32_t* __restrict__ cache_lengths,
                                              uint32_t B, uint32_t T, uint32_t* s_off,
                                              uint32_t* s_clen) {
-    for (uint32_t i = threadIdx.x; i <= B; i += blockDim.x) {
-        s_off[i] = __ldg(offsets + i);
-        if (i < B) s_clen[i] = __ldg(cache_lengths + i);
-    }
-    __syncthreads();
-    int ok = 1;
-    for (uint32_t i = threadIdx.x; i < B; i += blockDim.x)
-        if (s_off[i] > s_off[i + 1]) ok = 0;
-    if (threadIdx.x == 0 && (s_off[0] != 0u || s_off[B] != T)) ok = 0;
-    return __syncthreads_and(ok) != 0;
+    RaggedLoads r;
+    r.issue(offsets, cache_lengths, B);
+    return r.commit(offsets, cache_lengths, B, T, s_off, s_clen);
 }
 
 // Request owning token t, for validated offsets (offsets[0] = 0 <= t <
@@ -123,6 +174,16 @@ __device__ __forceinline__ uint32_t find_request(const uint32_t* s_off, uint32_t
             hi = mid;
     }
     return lo;
+}
+
+// Page id of slot `pos` of request b, or KVW_PAGE_UNMAPPED when the page
+// index is past the table (callers compare the result with num_pages).
+__device__ __forceinline__ uint32_t page_of(const uint32_t* __restrict__ page_table,
+                                           uint32_t max_pages, uint32_t page_size, uint32_t b,
+                                           uint64_t pos) {
+    const uint64_t pidx = pos / page_size;
+    return pidx < max_pages ? __ldg(page_table + (uint64_t)b * max_pages + pidx)
+                            : KVW_PAGE_UNMAPPED;
 }
 
 // Element offset of the K row of slot `pos` of request b in `layer_off`, or

@@ -59,7 +59,7 @@ __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&
     if constexpr (FP8) {
         float z[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) z[i] = __fdiv_rn(y[i], scale);
+        for (int i = 0; i < 8; ++i) z[i] = scale == 1.0f ? y[i] : __fdiv_rn(y[i], scale);
         *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) = pack8_e4m3(z);
     } else {
         *reinterpret_cast<uint4*>(static_cast<uint16_t*>(cache) + elem) = pack8_bf16(y);
@@ -67,12 +67,17 @@ __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&
 }
 
 // One warp per token: RMSNorm of the latent part, RoPE of the rope part,
-// quantise, write the 576-wide cache row.
+// quantise, write the 576-wide cache row.  Memory order: ragged tables first
+// (they gate everything position-dependent), then the row and gamma; the
+// norm is computed while the tables are in flight; the page id and the freqs
+// slice (both need only the position) are then loaded together.
 template <bool FP8>
 __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
     const bool active = t < a.T;
+    RaggedLoads rl;
+    rl.issue(a.offsets, a.cache_lengths, a.B);
     uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
     if (active) {
         const uint4* row = reinterpret_cast<const uint4*>(a.kv_in + (int64_t)t * a.kv_row_stride);
@@ -82,30 +87,7 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         g0 = ld_table(a.gamma + lane);
         g1 = ld_table(a.gamma + 32 + lane);
     }
-    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
-        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
-        return;
-    }
-    if (!active) return;
-    const uint32_t b = find_request(s_off, a.B, t);
-    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-    if (pos >= a.freqs_rows) {
-        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
-        return;
-    }
-    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
-                                  a.s_token, a.layer_off, b, pos);
-    if (base < 0) {
-        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
-        return;
-    }
-    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
-    if (lane < 8) {
-        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
-        fa = ld_table(fr);
-        fb = ld_table(fr + 1);
-    }
-    // RMSNorm of the 512 latent values held 16 per lane.
+    // RMSNorm of the 512 latent values held 16 per lane (position-free).
     float v0[8], v1[8], w0[8], w1[8];
     unpack8(x0, v0);
     unpack8(x1, v1);
@@ -125,6 +107,30 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         y0[i] = __fmul_rn(__fmul_rn(v0[i], r), w0[i]);
         y1[i] = __fmul_rn(__fmul_rn(v1[i], r), w1[i]);
     }
+    if (!rl.commit(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    if (!active) return;
+    const uint32_t b = find_request(s_off, a.B, t);
+    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+    if (pos >= a.freqs_rows) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
+        return;
+    }
+    const uint32_t page = page_of(a.page_table, a.max_pages, a.page_size, b, pos);
+    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+    if (lane < 8) {
+        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
+        fa = ld_table(fr);
+        fb = ld_table(fr + 1);
+    }
+    if (page >= a.num_pages) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
+        return;
+    }
+    const int64_t base =
+        (int64_t)page * a.s_page + a.layer_off + (int64_t)(pos % a.page_size) * a.s_token;
     store8<FP8>(a.cache, base + lane * 8, y0, a.scale);
     store8<FP8>(a.cache, base + 256 + lane * 8, y1, a.scale);
     if (lane < 8) {  // rope part: 4 adjacent pairs per lane
@@ -138,12 +144,16 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
     }
 }
 
-// q_rope streaming: VPT 16-byte vectors per thread.
+// q_rope streaming: VPT 16-byte vectors per thread.  After the one barrier
+// of the ragged staging, each thread resolves the position of its own token
+// (binary search in shared memory, once per distinct token), so no further
+// block-wide synchronisation is needed.
 template <int VPT>
 __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
-    __shared__ uint32_t s_pos[(kThreads * VPT) / 8 + 2];
     const uint32_t qb = blockIdx.x - a.kv_blocks;
     const uint32_t vbase = qb * (kThreads * VPT);
+    RaggedLoads rl;
+    rl.issue(a.offsets, a.cache_lengths, a.B);
     uint4 x[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) x[i] = make_uint4(0, 0, 0, 0);
@@ -152,28 +162,14 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
         const uint32_t v = vbase + threadIdx.x + i * kThreads;
         if (v < a.q_vectors) x[i] = ld_stream(a.q_in + v);
     }
-    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+    if (!rl.commit(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-    const uint32_t vpt = a.H * 8u;  // vectors per token
-    const uint32_t t0 = vbase / vpt;
-    const uint32_t vlast = min(vbase + kThreads * VPT, a.q_vectors) - 1u;
-    const uint32_t ntok = vlast / vpt - t0 + 1u;
-    for (uint32_t k = threadIdx.x; k < ntok; k += kThreads) {
-        const uint32_t t = t0 + k;
-        const uint32_t b = find_request(s_off, a.B, t);
-        const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-        if (pos >= a.freqs_rows) {
-            s_pos[k] = 0xffffffffu;
-            flag(a.err_flags, KVW_ERR_POSITION);
-        } else {
-            s_pos[k] = (uint32_t)pos;
-        }
-    }
-    __syncthreads();
+    const uint32_t vpt = a.H * 8u;        // vectors per token
     const uint32_t j = threadIdx.x & 7u;  // 8-column slice of the 64-wide head row
-    uint32_t cur_t = 0xffffffffu, p = 0xffffffffu;
+    uint32_t cur_t = 0xffffffffu;
+    bool ok = false;
     float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -182,14 +178,18 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
         const uint32_t t = v / vpt;
         if (t != cur_t) {
             cur_t = t;
-            p = s_pos[t - t0];
-            if (p != 0xffffffffu) {
-                const float4* fr = reinterpret_cast<const float4*>(a.freqs + (uint64_t)p * kRope) + j * 2;
+            const uint32_t b = find_request(s_off, a.B, t);
+            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+            ok = pos < a.freqs_rows;
+            if (ok) {
+                const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + j * 2;
                 fa = ld_table(fr);
                 fb = ld_table(fr + 1);
+            } else if ((v % vpt) == 0) {
+                flag(a.err_flags, KVW_ERR_POSITION);
             }
         }
-        if (p == 0xffffffffu) continue;
+        if (!ok) continue;
         float xv[8], y[8];
         unpack8(x[i], xv);
         rope_pair(xv[0], xv[1], fa.x, fa.y, y[0], y[1]);
@@ -220,6 +220,40 @@ cudaError_t launch(const MlaArgs& a, uint32_t blocks, size_t smem, cudaStream_t 
     }
     k<<<blocks, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+// CTAs of this kernel that fit on the device at once (all SMs).
+template <bool FP8, int VPT>
+uint64_t resident_ctas(size_t smem) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, mla_rope_rmsnorm_quant_kernel<FP8, VPT>, kThreads, smem) != cudaSuccess)
+        return 0;
+    return (uint64_t)sms * (uint64_t)per_sm;
+}
+
+template <bool FP8>
+cudaError_t launch_sized(const MlaArgs& a, uint64_t qvec, size_t smem, cudaStream_t stream) {
+    // Vectors per thread: the smallest of 1, 2, 4 whose grid fits in one wave
+    // of resident CTAs (a decode step is latency-bound: a second wave would
+    // double its duration); 4 when nothing fits (long prefill launches).
+    int vpt = 4;
+    for (int cand : {1, 2}) {
+        const uint64_t qblocks = (qvec + (uint64_t)kThreads * cand - 1) / ((uint64_t)kThreads * cand);
+        const uint64_t cap = cand == 1 ? resident_ctas<FP8, 1>(smem) : resident_ctas<FP8, 2>(smem);
+        if (a.kv_blocks + qblocks <= cap) {
+            vpt = cand;
+            break;
+        }
+    }
+    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
+    const uint64_t blocks = a.kv_blocks + qblocks;
+    if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+    return vpt == 1 ? launch<FP8, 1>(a, (uint32_t)blocks, smem, stream)
+         : vpt == 2 ? launch<FP8, 2>(a, (uint32_t)blocks, smem, stream)
+                    : launch<FP8, 4>(a, (uint32_t)blocks, smem, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -291,23 +325,8 @@ extern "C" int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, c
     a.eps = epsilon;
     a.scale = cache->scale;
 
-    // Vectors per thread: small launches (decode) use 1 so that the q work
-    // spreads over every SM; large ones use 4 to keep 64 B per thread in flight.
-    int vpt = 4;
-    if (qvec < 152ull * 8 * kThreads * 4) vpt = (qvec < 152ull * 4 * kThreads * 2) ? 1 : 2;
-    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
-    const uint64_t blocks = a.kv_blocks + qblocks;
-    if (blocks > 0x7fffffffull) return KVW_EUNSUPPORTED;
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
-    cudaError_t e;
-    if (fp8) {
-        e = vpt == 4 ? launch<true, 4>(a, (uint32_t)blocks, smem, stream)
-          : vpt == 2 ? launch<true, 2>(a, (uint32_t)blocks, smem, stream)
-                     : launch<true, 1>(a, (uint32_t)blocks, smem, stream);
-    } else {
-        e = vpt == 4 ? launch<false, 4>(a, (uint32_t)blocks, smem, stream)
-          : vpt == 2 ? launch<false, 2>(a, (uint32_t)blocks, smem, stream)
-                     : launch<false, 1>(a, (uint32_t)blocks, smem, stream);
-    }
+    const cudaError_t e = fp8 ? launch_sized<true>(a, qvec, smem, stream)
+                              : launch_sized<false>(a, qvec, smem, stream);
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }
