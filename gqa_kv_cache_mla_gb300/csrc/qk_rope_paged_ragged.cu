@@ -7,20 +7,29 @@
 // has_position_ids, mrope_section; Args q_proj, input_row_offsets,
 // kv_collection, freqs_cis, position_ids, layer_idx, output).
 //
-// GB300 design.  A token is (Hq + Hk) heads x head_size/16 "items"; an item
-// is 8 rotary pairs = two 16-byte vectors (adjacent for interleaved pairs,
-// k and k + head_size/2 for half-split pairs).  The CTA has one thread per
-// item of a token (rounded up to whole warps), so a thread's head and pair
-// range never change, and it walks TPB consecutive tokens:
-//   phase 0  query threads issue all their q_proj loads (TPB x 32 B);
-//   phase 1  offsets/cache_lengths staged and validated in shared memory;
-//   phase 2  per token: slot position and page lookup, and the token's
-//            composed freqs row (pair k read from the row of its own
-//            position, which covers plain, position_ids and mrope cases) is
-//            gathered once into shared memory;
-//   phase 3  key threads load their slot rows, everybody rotates and stores.
-// Every rotation is done in fp32 with separately rounded products and the
-// result is rounded once to bf16.
+// GB300 design: a persistent, warp-specialised TMA pipeline.
+//   * The tokens are cut into groups of TPB consecutive tokens; each CTA (one
+//     per SM, sized by shared memory) walks groups blockIdx.x, + gridDim.x, ...
+//   * A producer warp resolves each group's tokens (request by binary search
+//     in the staged offsets, slot position, RoPE positions, page id) and
+//     issues bulk (TMA) copies into a 2-stage shared-memory ring: the group's
+//     q_proj rows (one copy, they are contiguous), each token's K rows (one
+//     copy when the kv heads are contiguous) and the spans of freqs_cis rows
+//     the token's pairs use (one row, or the three mrope rows' sections).
+//     Copies complete on the stage's "full" mbarrier with a transaction
+//     count, so no thread waits on individual loads.
+//   * Eight consumer warps wait for the stage, rotate from shared memory and
+//     store straight to global memory (query rows to `output`, key rows back
+//     to their slots), then release the stage on its "empty" mbarrier.  A
+//     consumer thread owns one (token, 8-pair group, head slice): it reads the
+//     group's 8 (cos, sin) pairs once and applies them to every head of its
+//     slice.
+// While the consumers work on one group, the copy engine is already filling
+// the other stage, so every SM keeps tens of kilobytes in flight without
+// holding them in registers.  Every wait is bounded (about one second) and
+// reports KVW_ERR_TIMEOUT instead of hanging.
+// Rotation arithmetic: fp32, separately rounded products, one rounding to
+// bf16.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -29,6 +38,11 @@ namespace kvw {
 namespace {
 
 constexpr uint32_t kMaxHead = 512;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kStages = 2;
+constexpr uint32_t kMaxTPB = 16;
 
 struct GqaArgs {
     const uint16_t* q_in;  // bf16 [T, Hq, S]
@@ -42,157 +56,249 @@ struct GqaArgs {
     uint32_t* err_flags;
     int64_t s_page, s_token, s_head, layer_off;
     uint32_t B, T, Hq, Hk, S, freqs_rows, max_pages, num_pages, page_size;
-    uint32_t mode;         // 0: slot positions, 1: position_ids[T], 2: mrope [3, T]
-    uint32_t sec0, sec01;  // mrope section ends, in pairs
-    uint32_t items;        // (Hq + Hk) * S / 16
+    uint32_t mode;              // 0: slot positions, 1: position_ids[T], 2: mrope [3, T]
+    uint32_t sec0, sec01;       // mrope section ends, in pairs
+    uint32_t R;                 // freqs rows kept per token (1, or 3 for mrope)
+    uint32_t span_lo[3], span_hi[3];  // pair span copied from each row (even bounds)
+    uint32_t tpb, groups;       // tokens per group, number of groups
+    uint32_t heads_contig;      // kv heads adjacent (stride_head == S)
+    uint32_t tables_bytes;      // shared bytes of the staged ragged tables (x128)
+    uint32_t stage_bytes, q_off, k_off, f_off, meta_off;  // stage layout
+    uint32_t slices;            // head slices per (token, pair group)
 };
 
 __device__ __forceinline__ uint32_t section_of(const GqaArgs& a, uint32_t k) {
     return k < a.sec0 ? 0u : (k < a.sec01 ? 1u : 2u);
 }
 
-template <bool INTERLEAVED, int TPB>
-__global__ void __launch_bounds__(1024) qk_rope_kernel(const GqaArgs a) {
-    extern __shared__ uint32_t s_dyn[];
-    uint32_t* s_off = s_dyn;
-    uint32_t* s_clen = s_dyn + a.B + 1;
-    __shared__ __align__(16) float s_cs[TPB][kMaxHead];  // composed (cos, sin) per pair
-    __shared__ int64_t s_kbase[TPB];
-    __shared__ int s_bad[TPB];
+struct TokMeta {
+    int64_t kbase;  // element offset of the K row (head 0), -1: not written
+    uint32_t qok;   // RoPE positions valid: query and key rows may be written
+    uint32_t pad;
+};
 
-    const uint32_t groups = a.S >> 4;  // items per head
-    const uint32_t i = threadIdx.x;
-    const bool has_item = i < a.items;
-    const uint32_t h = has_item ? i / groups : 0u;
-    const uint32_t m = has_item ? i % groups : 0u;
-    const bool is_q = has_item && h < a.Hq;
-    const uint32_t t_begin = blockIdx.x * TPB;
-    // element offsets of the two vectors of this item inside a head row
-    const uint32_t e0 = INTERLEAVED ? 16u * m : 8u * m;
-    const uint32_t e1 = INTERLEAVED ? 16u * m + 8u : (a.S >> 1) + 8u * m;
-
-    if (i < TPB) s_bad[i] = 0;
-
-    // phase 0: query data
-    uint4 xa[TPB], xb[TPB];
+__device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint64_t* empty,
+                                         const uint32_t* s_off, const uint32_t* s_clen,
+                                         unsigned char* stages) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t row_bytes = a.S * 2u;
+    uint32_t it = 0;
+    for (uint32_t g = blockIdx.x; g < a.groups; g += gridDim.x, ++it) {
+        const uint32_t s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        if (it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+            if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
+            break;
+        }
+        unsigned char* st = stages + (size_t)s * a.stage_bytes;
+        TokMeta* meta = reinterpret_cast<TokMeta*>(st + a.meta_off);
+        const uint32_t t0 = g * a.tpb;
+        const uint32_t ntok = min(a.tpb, a.T - t0);
+        uint64_t p[3] = {0, 0, 0};
+        int64_t kbase = -1;
+        uint32_t qok = 0, bytes = 0;
+        if (lane < ntok) {
+            const uint32_t t = t0 + lane;
+            const uint32_t b = find_request(s_off, a.B, t);
+            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+            qok = 1;
+            if (a.mode == 0) {
+                p[0] = pos;
+                qok = pos < a.freqs_rows;
+            } else if (a.mode == 1) {
+                p[0] = __ldg(a.position_ids + t);
+                qok = p[0] < a.freqs_rows;
+            } else {
 #pragma unroll
-    for (int u = 0; u < TPB; ++u) {
-        xa[u] = make_uint4(0, 0, 0, 0);
-        xb[u] = xa[u];
-        const uint32_t t = t_begin + u;
-        if (is_q && t < a.T) {
-            const uint16_t* row = a.q_in + ((uint64_t)t * a.Hq + h) * a.S;
-            xa[u] = ld_stream(reinterpret_cast<const uint4*>(row + e0));
-            xb[u] = ld_stream(reinterpret_cast<const uint4*>(row + e1));
+                for (int r = 0; r < 3; ++r) {
+                    if (a.span_hi[r] > a.span_lo[r]) {
+                        p[r] = __ldg(a.position_ids + (uint64_t)r * a.T + t);
+                        if (p[r] >= a.freqs_rows) qok = 0;
+                    }
+                }
+            }
+            if (!qok) {
+                flag(a.err_flags, KVW_ERR_POSITION);
+            } else {
+                kbase = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                                 a.s_token, a.layer_off, b, pos);
+                if (kbase < 0) flag(a.err_flags, KVW_ERR_PAGE);
+                for (uint32_t r = 0; r < a.R; ++r) bytes += (a.span_hi[r] - a.span_lo[r]) * 8u;
+                if (kbase >= 0) bytes += a.Hk * row_bytes;
+            }
+            meta[lane].kbase = kbase;
+            meta[lane].qok = qok;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        const uint32_t qbytes = ntok * a.Hq * row_bytes;
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes + qbytes);
+        __syncwarp();
+        if (lane == 0 && qbytes)
+            bulk_load(st + a.q_off, a.q_in + (uint64_t)t0 * a.Hq * a.S, qbytes, &full[s]);
+        if (lane < ntok && qok) {
+            if (kbase >= 0) {
+                unsigned char* kdst = st + a.k_off + (size_t)lane * a.Hk * row_bytes;
+                if (a.heads_contig) {
+                    bulk_load(kdst, a.cache + kbase, a.Hk * row_bytes, &full[s]);
+                } else {
+                    for (uint32_t h = 0; h < a.Hk; ++h)
+                        bulk_load(kdst + h * row_bytes, a.cache + kbase + (int64_t)h * a.s_head,
+                                  row_bytes, &full[s]);
+                }
+            }
+            for (uint32_t r = 0; r < a.R; ++r) {
+                const uint32_t lo = a.span_lo[r], hi = a.span_hi[r];
+                if (hi > lo)
+                    bulk_load(st + a.f_off + ((size_t)lane * a.R + r) * a.S * 4u + lo * 8u,
+                              a.freqs + p[r] * a.S + 2u * lo, (hi - lo) * 8u, &full[s]);
+            }
         }
     }
+    // Do not leave the CTA with copies in flight: wait for the stages issued last.
+    if (lane == 0) {
+        for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0u; j < it; ++j)
+            if (!mbar_wait(&full[j % kStages], (j / kStages) & 1u, kWaitLimitNs))
+                flag(a.err_flags, KVW_ERR_TIMEOUT);
+    }
+}
 
-    // phase 1: ragged metadata (contains a __syncthreads, so s_bad is ready)
+template <bool INTERLEAVED>
+__device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint64_t* empty,
+                                         const unsigned char* stages) {
+    const uint32_t tid = threadIdx.x, lane = tid & 31u;
+    const uint32_t G = a.S >> 4;  // 8-pair groups per head
+    const uint32_t H = a.Hq + a.Hk;
+    const uint32_t hps = (H + a.slices - 1) / a.slices;
+    const uint32_t units = a.tpb * G * a.slices;
+    // element offsets of the two 8-element vectors of pair group m in a head row
+    uint32_t it = 0;
+    for (uint32_t g = blockIdx.x; g < a.groups; g += gridDim.x, ++it) {
+        const uint32_t s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        if (!mbar_wait(&full[s], ph, kWaitLimitNs)) {
+            if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
+            return;
+        }
+        const unsigned char* st = stages + (size_t)s * a.stage_bytes;
+        const TokMeta* meta = reinterpret_cast<const TokMeta*>(st + a.meta_off);
+        const uint32_t t0 = g * a.tpb;
+        const uint32_t ntok = min(a.tpb, a.T - t0);
+        for (uint32_t w = tid; w < units; w += kConsumers) {
+            const uint32_t m = w % G;
+            const uint32_t rest = w / G;
+            const uint32_t sl = rest % a.slices;
+            const uint32_t u = rest / a.slices;
+            if (u >= ntok) continue;
+            const TokMeta tm = meta[u];
+            if (!tm.qok) continue;
+            const uint32_t h_begin = sl * hps;
+            const uint32_t h_end = min(H, h_begin + hps);
+            if (h_begin >= h_end) continue;
+            // (cos, sin) of pairs 8m .. 8m+7
+            float c[8], sn[8];
+            const float* frow = reinterpret_cast<const float*>(st + a.f_off) + (size_t)u * a.R * a.S;
+            if (a.mode != 2) {
+                const float4* f4 = reinterpret_cast<const float4*>(frow + 16u * m);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = f4[q];
+                    c[2 * q] = v.x;
+                    sn[2 * q] = v.y;
+                    c[2 * q + 1] = v.z;
+                    sn[2 * q + 1] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t k = 8u * m + q;
+                    const float2 v =
+                        *reinterpret_cast<const float2*>(frow + (size_t)section_of(a, k) * a.S + 2u * k);
+                    c[q] = v.x;
+                    sn[q] = v.y;
+                }
+            }
+            const uint32_t e0 = INTERLEAVED ? 16u * m : 8u * m;
+            const uint32_t e1 = INTERLEAVED ? 16u * m + 8u : (a.S >> 1) + 8u * m;
+            for (uint32_t h = h_begin; h < h_end; ++h) {
+                const bool is_q = h < a.Hq;
+                if (!is_q && tm.kbase < 0) break;
+                const uint16_t* src =
+                    is_q ? reinterpret_cast<const uint16_t*>(st + a.q_off) + ((size_t)u * a.Hq + h) * a.S
+                         : reinterpret_cast<const uint16_t*>(st + a.k_off) +
+                               ((size_t)u * a.Hk + (h - a.Hq)) * a.S;
+                float va[8], vb[8], ya[8], yb[8];
+                unpack8(*reinterpret_cast<const uint4*>(src + e0), va);
+                unpack8(*reinterpret_cast<const uint4*>(src + e1), vb);
+                if (INTERLEAVED) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        rope_pair(va[2 * q], va[2 * q + 1], c[q], sn[q], ya[2 * q], ya[2 * q + 1]);
+                        rope_pair(vb[2 * q], vb[2 * q + 1], c[q + 4], sn[q + 4], yb[2 * q],
+                                  yb[2 * q + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) rope_pair(va[q], vb[q], c[q], sn[q], ya[q], yb[q]);
+                }
+                if (is_q) {
+                    uint16_t* dst = a.q_out + ((uint64_t)(t0 + u) * a.Hq + h) * a.S;
+                    st_stream(reinterpret_cast<uint4*>(dst + e0), pack8_bf16(ya));
+                    st_stream(reinterpret_cast<uint4*>(dst + e1), pack8_bf16(yb));
+                } else {
+                    uint16_t* dst = a.cache + tm.kbase + (int64_t)(h - a.Hq) * a.s_head;
+                    *reinterpret_cast<uint4*>(dst + e0) = pack8_bf16(ya);
+                    *reinterpret_cast<uint4*>(dst + e1) = pack8_bf16(yb);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+template <bool INTERLEAVED>
+__global__ void __launch_bounds__(kThreads, 1) qk_rope_kernel(const GqaArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kStages;
+    uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + 128);
+    uint32_t* s_clen = s_off + a.B + 1;
+    unsigned char* stages = smem + 128 + a.tables_bytes;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    // the barrier inside also publishes the mbarrier initialisation
     if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-
-    // phase 2a: slot row of each token
-    if (i < TPB) {
-        const uint32_t t = t_begin + i;
-        int64_t base = -1;
-        if (t < a.T) {
-            const uint32_t b = find_request(s_off, a.B, t);
-            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-            base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
-                            a.s_token, a.layer_off, b, pos);
-        }
-        s_kbase[i] = base;
-    }
-    // phase 2b: composed freqs rows, one (cos, sin) pair per rotary pair
-    const uint32_t half = a.S >> 1;
-    for (uint32_t idx = threadIdx.x; idx < TPB * half; idx += blockDim.x) {
-        const uint32_t u = idx / half, k = idx % half;
-        const uint32_t t = t_begin + u;
-        if (t >= a.T) continue;
-        uint64_t p;
-        if (a.mode == 0) {
-            const uint32_t b = find_request(s_off, a.B, t);
-            p = (uint64_t)s_clen[b] + (t - s_off[b]);
-        } else if (a.mode == 1) {
-            p = __ldg(a.position_ids + t);
-        } else {
-            p = __ldg(a.position_ids + (uint64_t)section_of(a, k) * a.T + t);
-        }
-        float2 cs = make_float2(0.f, 0.f);
-        if (p < a.freqs_rows)
-            cs = __ldg(reinterpret_cast<const float2*>(a.freqs + p * a.S) + k);
-        else
-            s_bad[u] = 1;
-        *reinterpret_cast<float2*>(&s_cs[u][2 * k]) = cs;
-    }
-    __syncthreads();
-
-    // phase 3a: key data (needs the slot rows)
-    if (has_item && !is_q) {
-#pragma unroll
-        for (int u = 0; u < TPB; ++u) {
-            const int64_t kb = s_kbase[u];
-            if (kb >= 0 && !s_bad[u]) {
-                const uint16_t* row = a.cache + kb + (int64_t)(h - a.Hq) * a.s_head;
-                xa[u] = *reinterpret_cast<const uint4*>(row + e0);
-                xb[u] = *reinterpret_cast<const uint4*>(row + e1);
-            }
-        }
-    }
-    if (i < TPB && t_begin + i < a.T) {
-        if (s_bad[i])
-            flag(a.err_flags, KVW_ERR_POSITION);
-        else if (s_kbase[i] < 0)
-            flag(a.err_flags, KVW_ERR_PAGE);
-    }
-    if (!has_item) return;
-
-    // phase 3b: rotate and store
-#pragma unroll
-    for (int u = 0; u < TPB; ++u) {
-        const uint32_t t = t_begin + u;
-        if (t >= a.T || s_bad[u]) continue;
-        if (!is_q && s_kbase[u] < 0) continue;
-        const float4* cs4 = reinterpret_cast<const float4*>(&s_cs[u][16u * m]);
-        const float4 c0 = cs4[0], c1 = cs4[1], c2 = cs4[2], c3 = cs4[3];
-        const float c[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
-        const float s[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
-        float va[8], vb[8], ya[8], yb[8];
-        unpack8(xa[u], va);
-        unpack8(xb[u], vb);
-        if (INTERLEAVED) {  // pairs (va0,va1) (va2,va3) .. (vb6,vb7)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                rope_pair(va[2 * q], va[2 * q + 1], c[q], s[q], ya[2 * q], ya[2 * q + 1]);
-                rope_pair(vb[2 * q], vb[2 * q + 1], c[q + 4], s[q + 4], yb[2 * q], yb[2 * q + 1]);
-            }
-        } else {  // pairs (va[q], vb[q])
-#pragma unroll
-            for (int q = 0; q < 8; ++q) rope_pair(va[q], vb[q], c[q], s[q], ya[q], yb[q]);
-        }
-        uint16_t* row = is_q ? a.q_out + ((uint64_t)t * a.Hq + h) * a.S
-                             : a.cache + s_kbase[u] + (int64_t)(h - a.Hq) * a.s_head;
-        if (is_q) {
-            st_stream(reinterpret_cast<uint4*>(row + e0), pack8_bf16(ya));
-            st_stream(reinterpret_cast<uint4*>(row + e1), pack8_bf16(yb));
-        } else {
-            *reinterpret_cast<uint4*>(row + e0) = pack8_bf16(ya);
-            *reinterpret_cast<uint4*>(row + e1) = pack8_bf16(yb);
-        }
-    }
+    if (threadIdx.x >= (unsigned)kConsumers)
+        producer(a, full, empty, s_off, s_clen, stages);
+    else
+        consumer<INTERLEAVED>(a, full, empty, stages);
 }
 
-template <bool INTERLEAVED, int TPB>
-cudaError_t launch(const GqaArgs& a, uint32_t threads, size_t smem, cudaStream_t stream) {
-    auto k = qk_rope_kernel<INTERLEAVED, TPB>;
-    if (smem > 16 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    const uint32_t blocks = (a.T + TPB - 1) / TPB;
-    k<<<blocks, threads, smem, stream>>>(a);
+template <bool INTERLEAVED>
+cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
+    auto k = qk_rope_kernel<INTERLEAVED>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const uint64_t cap = (uint64_t)sms * per_sm;
+    const uint32_t grid = (uint32_t)(a.groups < cap ? a.groups : cap);
+    k<<<grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -267,22 +373,54 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     a.mode = position_ids ? (mrope_section ? 2u : 1u) : 0u;
     a.sec0 = sec0;
     a.sec01 = sec01;
-    a.items = (uint32_t)items;
-
-    const uint32_t threads = (uint32_t)((items + 31) / 32 * 32);
-    const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
-    // Tokens per CTA: enough to keep >= 2 waves of CTAs over 152 SMs.
-    int tpb = 4;
-    while (tpb > 1 && (uint64_t)(tot_seq_len + tpb - 1) / tpb < 152ull * 4) tpb >>= 1;
-    cudaError_t e;
-    if (interleaved) {
-        e = tpb == 4 ? launch<true, 4>(a, threads, smem, stream)
-          : tpb == 2 ? launch<true, 2>(a, threads, smem, stream)
-                     : launch<true, 1>(a, threads, smem, stream);
+    if (a.mode == 2) {
+        // each mrope row only supplies its own section's pairs; copy that span
+        // widened to an even number of pairs (16-byte aligned, 16-byte sized)
+        const uint32_t lo[3] = {0u, sec0, sec01}, hi[3] = {sec0, sec01, S / 2};
+        a.R = 3;
+        for (int r = 0; r < 3; ++r) {
+            a.span_lo[r] = hi[r] > lo[r] ? (lo[r] & ~1u) : 0u;
+            a.span_hi[r] = hi[r] > lo[r] ? ((hi[r] + 1u) & ~1u) : 0u;
+        }
     } else {
-        e = tpb == 4 ? launch<false, 4>(a, threads, smem, stream)
-          : tpb == 2 ? launch<false, 2>(a, threads, smem, stream)
-                     : launch<false, 1>(a, threads, smem, stream);
+        a.R = 1;
+        a.span_lo[0] = 0;
+        a.span_hi[0] = S / 2;
+        a.span_lo[1] = a.span_hi[1] = a.span_lo[2] = a.span_hi[2] = 0;
     }
+    a.heads_contig = cache->stride_head == (int64_t)S ? 1u : 0u;
+
+    // shared memory: barriers | ragged tables | kStages x (q | k | freqs | meta)
+    const uint32_t tables = (uint32_t)(((2ull * num_batches + 1) * 4 + 127) / 128 * 128);
+    const uint64_t per_tok = (uint64_t)(num_q_heads + a.Hk) * S * 2 + (uint64_t)a.R * S * 4 +
+                             sizeof(TokMeta);
+    int dev = 0, optin = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KVW_ECUDA;
+    const uint64_t budget = (uint64_t)optin - 128 - tables - kStages * 1024;
+    uint64_t tpb = budget / (kStages * per_tok);
+    if (tpb > kMaxTPB) tpb = kMaxTPB;
+    // small batches: spread the groups over all SMs
+    const uint64_t spread = (tot_seq_len + (uint64_t)sms - 1) / sms;
+    if (tpb > spread) tpb = spread;
+    if (tpb == 0) return KVW_EUNSUPPORTED;
+    a.tpb = (uint32_t)tpb;
+    a.groups = (uint32_t)((tot_seq_len + tpb - 1) / tpb);
+    a.tables_bytes = tables;
+    auto up16 = [](uint64_t x) { return (uint32_t)((x + 15) / 16 * 16); };
+    a.q_off = 0;
+    a.k_off = up16(tpb * num_q_heads * S * 2);
+    a.f_off = a.k_off + up16(tpb * a.Hk * S * 2);
+    a.meta_off = a.f_off + up16(tpb * a.R * S * 4);
+    a.stage_bytes = (uint32_t)((a.meta_off + tpb * sizeof(TokMeta) + 127) / 128 * 128);
+    const uint32_t G = S / 16;
+    a.slices = (uint32_t)(kConsumers / (tpb * G));
+    if (a.slices < 1) a.slices = 1;
+    if (a.slices > num_q_heads + a.Hk) a.slices = num_q_heads + a.Hk;
+    const size_t smem = 128 + (size_t)tables + (size_t)kStages * a.stage_bytes;
+    if (smem > (size_t)optin) return KVW_EUNSUPPORTED;
+    const cudaError_t e = interleaved ? launch<true>(a, smem, stream) : launch<false>(a, smem, stream);
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }

@@ -86,6 +86,7 @@ class PagedCache:
     page_size: int
     num_heads: int
     head_size: int
+    custom_strides: Optional[tuple] = None  # (page, kv, layer, token, head), elements
 
     @property
     def max_pages_per_seq(self) -> int:
@@ -93,6 +94,8 @@ class PagedCache:
 
     @property
     def strides(self):
+        if self.custom_strides is not None:
+            return tuple(int(v) for v in self.custom_strides)
         s_head = self.head_size
         s_token = self.num_heads * s_head
         s_layer = self.page_size * s_token
@@ -104,9 +107,33 @@ class PagedCache:
     def elem_bytes(self) -> int:
         return 2 if self.dtype == DTYPE_BF16 else 1
 
-    def view6(self) -> np.ndarray:
-        return self.data.reshape(self.num_pages, self.kv_dim, self.num_layers,
-                                 self.page_size, self.num_heads, self.head_size)
+    def view6(self, data=None) -> np.ndarray:
+        """Logical [pages, kv, layers, page_size, heads, head_size] view of
+        ``data`` (default: this cache's bytes) under this cache's strides."""
+        d = self.data if data is None else data
+        eb = d.itemsize
+        shape = (self.num_pages, self.kv_dim, self.num_layers, self.page_size, self.num_heads,
+                 self.head_size)
+        return np.lib.stride_tricks.as_strided(d, shape=shape,
+                                               strides=tuple(eb * v for v in self.strides) + (eb,))
+
+
+def repad_cache(c: PagedCache, head_pad: int, token_pad: int, rng=None) -> PagedCache:
+    """The same logical cache in a padded layout: each head row is followed by
+    ``head_pad`` spare elements and each token row by ``token_pad``; spare
+    elements hold random bytes."""
+    rng = rng_for(12345) if rng is None else rng
+    s_head = c.head_size + head_pad
+    s_token = c.num_heads * s_head + token_pad
+    s_layer = c.page_size * s_token
+    s_kv = c.num_layers * s_layer
+    s_page = c.kv_dim * s_kv
+    n = c.num_pages * s_page
+    raw = rng.integers(0, 256, size=n * c.elem_bytes, dtype=np.uint8)
+    data = raw.view(np.uint16) if c.elem_bytes == 2 else raw
+    out = dataclasses.replace(c, data=data, custom_strides=(s_page, s_kv, s_layer, s_token, s_head))
+    out.view6()[...] = c.view6()
+    return out
 
 
 def build_page_table(rng, total_lens, page_size, max_pages_per_seq, whole=False,

@@ -32,6 +32,10 @@
  *                      is written;
  *     KVW_ERR_OFFSETS  input_row_offsets does not start at 0, does not end
  *                      at the token count, or decreases: nothing is written.
+ *     KVW_ERR_TIMEOUT  an internal pipeline wait (between the copy engine
+ *                      and the compute warps of one CTA) gave up after about
+ *                      one second; the output is incomplete.  Never expected;
+ *                      reported instead of hanging the GPU.
  *   With zero tokens nothing is launched and nothing is checked.
  * - Ragged batches: input_row_offsets (device, uint32 [num_batches + 1])
  *   marks request boundaries in the flattened token dimension; request b
@@ -65,7 +69,12 @@ enum kvw_status {
 
 enum kvw_dtype { KVW_DTYPE_BF16 = 0, KVW_DTYPE_FP8_E4M3 = 1, KVW_DTYPE_F32 = 2 };
 
-enum kvw_err_bits { KVW_ERR_PAGE = 1u, KVW_ERR_POSITION = 2u, KVW_ERR_OFFSETS = 4u };
+enum kvw_err_bits {
+    KVW_ERR_PAGE = 1u,
+    KVW_ERR_POSITION = 2u,
+    KVW_ERR_OFFSETS = 4u,
+    KVW_ERR_TIMEOUT = 8u
+};
 
 #define KVW_MAX_BATCHES 8192u
 #define KVW_PAGE_UNMAPPED 0xFFFFFFFFu

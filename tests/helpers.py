@@ -69,13 +69,20 @@ def compare_cache(cache, gpu, ref, slots, layer_idx, fp8, max_ulp_frac=None, col
     diff = np.flatnonzero(gpu != ref)
     if diff.size == 0:
         return 0
-    shape = (cache.num_pages, cache.kv_dim, cache.num_layers, cache.page_size, cache.num_heads,
-             cache.head_size)
-    page, kv, layer, row, head, col = np.unravel_index(diff, shape)
-    mask = written_row_mask(cache, slots, layer_idx)
-    inside = (kv == 0) & mask[page, layer, row]
-    if cols is not None:
-        inside &= col < cols
+    if cache.custom_strides is None:
+        shape = (cache.num_pages, cache.kv_dim, cache.num_layers, cache.page_size,
+                 cache.num_heads, cache.head_size)
+        page, kv, layer, row, head, col = np.unravel_index(diff, shape)
+        mask = written_row_mask(cache, slots, layer_idx)
+        inside = (kv == 0) & mask[page, layer, row]
+        if cols is not None:
+            inside &= col < cols
+    else:  # padded layout (small caches only): flat indices of the writable elements
+        flat = cache.view6(np.arange(gpu.size, dtype=np.int64))
+        allowed = np.zeros(gpu.size, dtype=bool)
+        for _, page, row, _ in slots:
+            allowed[flat[page, 0, layer_idx, row, :, : (cols or cache.head_size)].reshape(-1)] = True
+        inside = allowed[diff]
     assert inside.all(), "bytes changed outside the written rows: %d" % int((~inside).sum())
     if fp8:
         u = e4m3_ulp_diff(gpu[diff], ref[diff])

@@ -266,3 +266,48 @@ def test_knorm_error_flags(orc, dev):
     w.cache.page_table[1, 2] = W.PAGE_UNMAPPED  # positions 16..23 of request 1
     d = run_knorm(orc, dev, w)
     assert d.flags() == 1
+
+
+# ------------------------------------------------------------ padded layouts, small batches
+
+@pytest.mark.parametrize("kind", ["mla", "gqa", "gqa_mrope", "knorm"])
+def test_padded_cache_layouts(orc, dev, kind):
+    if kind == "mla":
+        w = W.mla_workload("p", 701, [3, 17, 1], [0, 40, 300], num_heads=16, page_size=16,
+                           max_seq_len=512, cache_dtype=W.DTYPE_BF16, num_layers=2, layer_idx=1)
+        w.cache = W.repad_cache(w.cache, 64, 0)
+        run_mla(orc, dev, w)
+    elif kind.startswith("gqa"):
+        mr = kind == "gqa_mrope"
+        w = W.gqa_workload("p", 702, [3, 17, 1], [0, 40, 300], 8, 4, 128, page_size=16,
+                           freqs_rows=512, base=500000.0, interleaved=not mr,
+                           position_mode="mrope" if mr else None,
+                           mrope_section=(16, 24, 24) if mr else None)
+        w.cache = W.repad_cache(w.cache, 16, 32)  # kv heads not adjacent: per-head copies
+        run_gqa(orc, dev, w)
+    else:
+        w = W.knorm_workload("p", 703, [3, 17, 1], [0, 40, 300], 4, 128, page_size=16,
+                             gamma_len=96)
+        w.cache = W.repad_cache(w.cache, 16, 32)
+        run_knorm(orc, dev, w)
+
+
+@pytest.mark.parametrize("new", [[1], [1, 1, 1], [5], [0, 2, 0, 0, 3], list(range(1, 40))])
+def test_gqa_small_and_single_token_batches(orc, dev, new):
+    prior = [7 * i for i in range(len(new))]
+    for interleaved in (True, False):
+        w = W.gqa_workload("t", 710 + len(new), new, prior, 32, 8, 128, page_size=64,
+                           freqs_rows=1024, base=500000.0, interleaved=interleaved,
+                           position_mode="ids")
+        run_gqa(orc, dev, w)
+
+
+def test_gqa_many_requests(orc, dev):
+    rng = np.random.default_rng(9)
+    B = 5000
+    new = rng.integers(0, 3, B)
+    prior = rng.integers(0, 500, B)
+    w = W.gqa_workload("m", 720, new, prior, 4, 2, 64, page_size=8, freqs_rows=1024,
+                       base=10000.0, interleaved=False, position_mode="mrope",
+                       mrope_section=(6, 13, 13))
+    run_gqa(orc, dev, w)

@@ -231,3 +231,39 @@ def test_openmp_threads_give_identical_results(orc):
     b = orc.mla_rope_rmsnorm_quant(w, nthreads=4)
     assert a[2] == b[2] == 0
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------ padded layouts
+
+def test_layout_independence(orc):
+    """The same logical cache in a padded layout (spare elements after every
+    head and token row) gives the same logical result, and the spare
+    elements are never touched."""
+    from helpers import bf16_to_f32  # noqa: F401
+
+    cases = [
+        ("mla", W.mla_tiny(cache_dtype=W.DTYPE_FP8_E4M3), 0, 32),
+        ("gqa", W.gqa_workload("p", 131, [3, 5, 1], [0, 7, 30], 4, 2, 32, page_size=16,
+                               freqs_rows=64, base=10000.0, interleaved=False,
+                               position_mode="mrope", mrope_section=(4, 6, 6)), 8, 16),
+        ("knorm", W.knorm_workload("p", 132, [3, 5, 1], [0, 7, 30], 3, 32, page_size=8,
+                                   gamma_len=24), 8, 24),
+    ]
+    for kind, w, head_pad, token_pad in cases:
+        dense = w.cache
+        padded = W.repad_cache(dense, head_pad, token_pad)
+        run = {"mla": orc.mla_rope_rmsnorm_quant, "gqa": orc.qk_rope_paged_ragged,
+               "knorm": orc.rms_norm_kv_cache_paged}[kind]
+        out_d = run(w)
+        w.cache = padded
+        out_p = run(w)
+        cache_d, cache_p = out_d[-2], out_p[-2]
+        assert out_d[-1] == out_p[-1] == 0
+        assert np.array_equal(dense.view6(cache_d), padded.view6(cache_p))
+        if kind != "knorm":
+            assert np.array_equal(out_d[0], out_p[0])
+        # spare elements untouched
+        n = padded.data.size
+        used = np.zeros(n, dtype=bool)
+        used[padded.view6(np.arange(n, dtype=np.int64)).reshape(-1)] = True
+        assert np.array_equal(cache_p[~used], padded.data[~used])
