@@ -91,17 +91,12 @@ __device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
 
 // ------------------------------------------------------------ ragged lookup
 
-// Ragged metadata staging, split in two so a kernel can put the table loads
-// at the head of its memory traffic:
-//   RaggedLoads r; r.issue(...)   loads offsets[i], offsets[i+1] and
-//                                 cache_lengths[i] for the first kRegRounds
-//                                 slices of the table into registers;
-//   ...                           the kernel issues its bulk loads here;
-//   r.commit(...)                 writes the shared copy (looping over any
-//                                 remainder), checks that the offsets start at
-//                                 0, never decrease and end at T, and returns
-//                                 that verdict through one barrier.
-// Every thread of the CTA must call both; the verdict is uniform.
+// Ragged metadata staging for the pipelined kernels (GQA, K norm): each
+// thread loads its slices of offsets[i], offsets[i+1] and cache_lengths[i]
+// into registers (issue), then writes the shared copy, checks that the
+// offsets start at 0, never decrease and end at T, and returns that verdict
+// through one barrier (commit).  Every thread of the CTA must call both; the
+// verdict is uniform.
 struct RaggedLoads {
     static constexpr int kRegRounds = 2;
     uint32_t off[kRegRounds], nxt[kRegRounds], clen[kRegRounds];
@@ -151,7 +146,7 @@ struct RaggedLoads {
     }
 };
 
-// Both halves at once, for kernels with nothing to overlap.
+// Both halves at once.
 __device__ __forceinline__ bool stage_ragged(const uint32_t* __restrict__ offsets,
                                              const uint32_t* __restrict__ cache_lengths,
                                              uint32_t B, uint32_t T, uint32_t* s_off,

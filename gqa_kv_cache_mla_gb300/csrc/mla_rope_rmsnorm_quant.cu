@@ -54,6 +54,27 @@ struct MlaArgs {
     float eps, scale;
 };
 
+// Stage offsets[0..B] and cache_lengths[0..B-1] in shared memory and check
+// that the offsets start at 0, never decrease and end at T (uniform verdict).
+// Copy, barrier, check from shared memory, barrier: for the many short CTAs
+// of a prefill launch this form measured faster than checking from
+// registers before a single barrier.
+__device__ __forceinline__ bool stage_tables(const uint32_t* __restrict__ offsets,
+                                             const uint32_t* __restrict__ cache_lengths,
+                                             uint32_t B, uint32_t T, uint32_t* s_off,
+                                             uint32_t* s_clen) {
+    for (uint32_t i = threadIdx.x; i <= B; i += blockDim.x) {
+        s_off[i] = __ldg(offsets + i);
+        if (i < B) s_clen[i] = __ldg(cache_lengths + i);
+    }
+    __syncthreads();
+    int ok = 1;
+    for (uint32_t i = threadIdx.x; i < B; i += blockDim.x)
+        if (s_off[i] > s_off[i + 1]) ok = 0;
+    if (threadIdx.x == 0 && (s_off[0] != 0u || s_off[B] != T)) ok = 0;
+    return __syncthreads_and(ok) != 0;
+}
+
 template <bool FP8>
 __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&y)[8], float scale) {
     if constexpr (FP8) {
@@ -67,17 +88,12 @@ __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&
 }
 
 // One warp per token: RMSNorm of the latent part, RoPE of the rope part,
-// quantise, write the 576-wide cache row.  Memory order: ragged tables first
-// (they gate everything position-dependent), then the row and gamma; the
-// norm is computed while the tables are in flight; the page id and the freqs
-// slice (both need only the position) are then loaded together.
+// quantise, write the 576-wide cache row.
 template <bool FP8>
 __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
     const bool active = t < a.T;
-    RaggedLoads rl;
-    rl.issue(a.offsets, a.cache_lengths, a.B);
     uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
     if (active) {
         const uint4* row = reinterpret_cast<const uint4*>(a.kv_in + (int64_t)t * a.kv_row_stride);
@@ -87,7 +103,30 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         g0 = ld_table(a.gamma + lane);
         g1 = ld_table(a.gamma + 32 + lane);
     }
-    // RMSNorm of the 512 latent values held 16 per lane (position-free).
+    if (!stage_tables(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    if (!active) return;
+    const uint32_t b = find_request(s_off, a.B, t);
+    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+    if (pos >= a.freqs_rows) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
+        return;
+    }
+    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                                  a.s_token, a.layer_off, b, pos);
+    if (base < 0) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
+        return;
+    }
+    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+    if (lane < 8) {
+        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
+        fa = ld_table(fr);
+        fb = ld_table(fr + 1);
+    }
+    // RMSNorm of the 512 latent values held 16 per lane.
     float v0[8], v1[8], w0[8], w1[8];
     unpack8(x0, v0);
     unpack8(x1, v1);
@@ -107,30 +146,6 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         y0[i] = __fmul_rn(__fmul_rn(v0[i], r), w0[i]);
         y1[i] = __fmul_rn(__fmul_rn(v1[i], r), w1[i]);
     }
-    if (!rl.commit(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
-        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
-        return;
-    }
-    if (!active) return;
-    const uint32_t b = find_request(s_off, a.B, t);
-    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-    if (pos >= a.freqs_rows) {
-        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
-        return;
-    }
-    const uint32_t page = page_of(a.page_table, a.max_pages, a.page_size, b, pos);
-    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
-    if (lane < 8) {
-        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
-        fa = ld_table(fr);
-        fb = ld_table(fr + 1);
-    }
-    if (page >= a.num_pages) {
-        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
-        return;
-    }
-    const int64_t base =
-        (int64_t)page * a.s_page + a.layer_off + (int64_t)(pos % a.page_size) * a.s_token;
     store8<FP8>(a.cache, base + lane * 8, y0, a.scale);
     store8<FP8>(a.cache, base + 256 + lane * 8, y1, a.scale);
     if (lane < 8) {  // rope part: 4 adjacent pairs per lane
@@ -144,16 +159,12 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
     }
 }
 
-// q_rope streaming: VPT 16-byte vectors per thread.  After the one barrier
-// of the ragged staging, each thread resolves the position of its own token
-// (binary search in shared memory, once per distinct token), so no further
-// block-wide synchronisation is needed.
+// q_rope streaming: VPT 16-byte vectors per thread.
 template <int VPT>
 __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
+    __shared__ uint32_t s_pos[(kThreads * VPT) / 8 + 2];
     const uint32_t qb = blockIdx.x - a.kv_blocks;
     const uint32_t vbase = qb * (kThreads * VPT);
-    RaggedLoads rl;
-    rl.issue(a.offsets, a.cache_lengths, a.B);
     uint4 x[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) x[i] = make_uint4(0, 0, 0, 0);
@@ -162,14 +173,28 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
         const uint32_t v = vbase + threadIdx.x + i * kThreads;
         if (v < a.q_vectors) x[i] = ld_stream(a.q_in + v);
     }
-    if (!rl.commit(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+    if (!stage_tables(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-    const uint32_t vpt = a.H * 8u;        // vectors per token
+    const uint32_t vpt = a.H * 8u;  // vectors per token
+    const uint32_t t0 = vbase / vpt;
+    const uint32_t vlast = min(vbase + kThreads * VPT, a.q_vectors) - 1u;
+    const uint32_t ntok = vlast / vpt - t0 + 1u;
+    for (uint32_t k = threadIdx.x; k < ntok; k += kThreads) {
+        const uint32_t t = t0 + k;
+        const uint32_t b = find_request(s_off, a.B, t);
+        const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+        if (pos >= a.freqs_rows) {
+            s_pos[k] = 0xffffffffu;
+            flag(a.err_flags, KVW_ERR_POSITION);
+        } else {
+            s_pos[k] = (uint32_t)pos;
+        }
+    }
+    __syncthreads();
     const uint32_t j = threadIdx.x & 7u;  // 8-column slice of the 64-wide head row
-    uint32_t cur_t = 0xffffffffu;
-    bool ok = false;
+    uint32_t cur_t = 0xffffffffu, p = 0xffffffffu;
     float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -178,18 +203,14 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
         const uint32_t t = v / vpt;
         if (t != cur_t) {
             cur_t = t;
-            const uint32_t b = find_request(s_off, a.B, t);
-            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-            ok = pos < a.freqs_rows;
-            if (ok) {
-                const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + j * 2;
+            p = s_pos[t - t0];
+            if (p != 0xffffffffu) {
+                const float4* fr = reinterpret_cast<const float4*>(a.freqs + (uint64_t)p * kRope) + j * 2;
                 fa = ld_table(fr);
                 fb = ld_table(fr + 1);
-            } else if ((v % vpt) == 0) {
-                flag(a.err_flags, KVW_ERR_POSITION);
             }
         }
-        if (!ok) continue;
+        if (p == 0xffffffffu) continue;
         float xv[8], y[8];
         unpack8(x[i], xv);
         rope_pair(xv[0], xv[1], fa.x, fa.y, y[0], y[1]);
@@ -232,28 +253,6 @@ uint64_t resident_ctas(size_t smem) {
             &per_sm, mla_rope_rmsnorm_quant_kernel<FP8, VPT>, kThreads, smem) != cudaSuccess)
         return 0;
     return (uint64_t)sms * (uint64_t)per_sm;
-}
-
-template <bool FP8>
-cudaError_t launch_sized(const MlaArgs& a, uint64_t qvec, size_t smem, cudaStream_t stream) {
-    // Vectors per thread: the smallest of 1, 2, 4 whose grid fits in one wave
-    // of resident CTAs (a decode step is latency-bound: a second wave would
-    // double its duration); 4 when nothing fits (long prefill launches).
-    int vpt = 4;
-    for (int cand : {1, 2}) {
-        const uint64_t qblocks = (qvec + (uint64_t)kThreads * cand - 1) / ((uint64_t)kThreads * cand);
-        const uint64_t cap = cand == 1 ? resident_ctas<FP8, 1>(smem) : resident_ctas<FP8, 2>(smem);
-        if (a.kv_blocks + qblocks <= cap) {
-            vpt = cand;
-            break;
-        }
-    }
-    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
-    const uint64_t blocks = a.kv_blocks + qblocks;
-    if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-    return vpt == 1 ? launch<FP8, 1>(a, (uint32_t)blocks, smem, stream)
-         : vpt == 2 ? launch<FP8, 2>(a, (uint32_t)blocks, smem, stream)
-                    : launch<FP8, 4>(a, (uint32_t)blocks, smem, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -325,8 +324,33 @@ extern "C" int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, c
     a.eps = epsilon;
     a.scale = cache->scale;
 
+    // Vectors per thread: the smallest of 1, 2, 4 whose grid fits in one wave
+    // of resident CTAs (a decode step is latency-bound: a second wave would
+    // double its duration); 4 when nothing fits (long prefill launches, where
+    // many short CTAs keep the memory system busy).
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
-    const cudaError_t e = fp8 ? launch_sized<true>(a, qvec, smem, stream)
-                              : launch_sized<false>(a, qvec, smem, stream);
+    int vpt = 4;
+    for (int cand : {1, 2}) {
+        const uint64_t qb = (qvec + (uint64_t)kThreads * cand - 1) / ((uint64_t)kThreads * cand);
+        const uint64_t cap = fp8 ? (cand == 1 ? resident_ctas<true, 1>(smem) : resident_ctas<true, 2>(smem))
+                                 : (cand == 1 ? resident_ctas<false, 1>(smem) : resident_ctas<false, 2>(smem));
+        if (a.kv_blocks + qb <= cap) {
+            vpt = cand;
+            break;
+        }
+    }
+    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
+    const uint64_t blocks = a.kv_blocks + qblocks;
+    if (blocks > 0x7fffffffull) return KVW_EUNSUPPORTED;
+    cudaError_t e;
+    if (fp8) {
+        e = vpt == 4 ? launch<true, 4>(a, (uint32_t)blocks, smem, stream)
+          : vpt == 2 ? launch<true, 2>(a, (uint32_t)blocks, smem, stream)
+                     : launch<true, 1>(a, (uint32_t)blocks, smem, stream);
+    } else {
+        e = vpt == 4 ? launch<false, 4>(a, (uint32_t)blocks, smem, stream)
+          : vpt == 2 ? launch<false, 2>(a, (uint32_t)blocks, smem, stream)
+                     : launch<false, 1>(a, (uint32_t)blocks, smem, stream);
+    }
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }

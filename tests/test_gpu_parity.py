@@ -311,3 +311,30 @@ def test_gqa_many_requests(orc, dev):
                        base=10000.0, interleaved=False, position_mode="mrope",
                        mrope_section=(6, 13, 13))
     run_gqa(orc, dev, w)
+
+
+# ------------------------------------------------------------ MLA streaming (large batch) path
+
+@pytest.mark.parametrize("H", [0, 1, 3, 5, 128])
+@pytest.mark.parametrize("dtype", [W.DTYPE_FP8_E4M3, W.DTYPE_BF16])
+def test_mla_stream_path_shapes(orc, dev, H, dtype):
+    rng = np.random.default_rng(800 + H)
+    new = rng.integers(500, 4000, 9)
+    new[2] = 0
+    new[5] = 1
+    prior = rng.integers(0, 3000, 9)
+    w = W.mla_workload("st", 801 + H, new, prior, num_heads=H, page_size=64,
+                       max_seq_len=8192, cache_dtype=dtype, num_layers=2, layer_idx=1)
+    run_mla(orc, dev, w)
+
+
+def test_mla_stream_path_flags(orc, dev):
+    rng = np.random.default_rng(811)
+    new = rng.integers(2000, 4000, 6)
+    prior = np.array([0, 100, 7000, 50, 6000, 10])
+    w = W.mla_workload("sf", 812, new, prior, num_heads=16, page_size=64, max_seq_len=12288,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    w.freqs = w.freqs[:8192].copy()  # requests 2 and 4 run past the table
+    w.cache.page_table[1, 3] = W.PAGE_UNMAPPED
+    d, _, _ = run_mla(orc, dev, w)
+    assert d.flags() == 3
