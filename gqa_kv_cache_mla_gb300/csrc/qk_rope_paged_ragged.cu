@@ -7,7 +7,9 @@
 // has_position_ids, mrope_section; Args q_proj, input_row_offsets,
 // kv_collection, freqs_cis, position_ids, layer_idx, output).
 //
-// GB300 design: a persistent, warp-specialised TMA pipeline.
+// GB300 design (slot positions and position_ids; mrope uses the
+// register-staged kernel further down): a persistent, warp-specialised TMA
+// pipeline.
 //   * The tokens are cut into groups of TPB consecutive tokens; each CTA (one
 //     per SM, sized by shared memory) walks groups blockIdx.x, + gridDim.x, ...
 //   * A producer warp resolves each group's tokens (request by binary search
@@ -62,9 +64,11 @@ struct GqaArgs {
     uint32_t span_lo[3], span_hi[3];  // pair span copied from each row (even bounds)
     uint32_t tpb, groups;       // tokens per group, number of groups
     uint32_t heads_contig;      // kv heads adjacent (stride_head == S)
+    uint32_t rows_contig;       // token rows adjacent too (stride_token == Hk * S)
     uint32_t tables_bytes;      // shared bytes of the staged ragged tables (x128)
     uint32_t stage_bytes, q_off, k_off, f_off, meta_off;  // stage layout
     uint32_t slices;            // head slices per (token, pair group)
+    uint32_t items;             // (Hq + Hk) * S / 16 (register-staged kernel)
 };
 
 __device__ __forceinline__ uint32_t section_of(const GqaArgs& a, uint32_t k) {
@@ -138,10 +142,30 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
         __syncwarp();
         if (lane == 0 && qbytes)
             bulk_load(st + a.q_off, a.q_in + (uint64_t)t0 * a.Hq * a.S, qbytes, &full[s]);
+        // K rows: one copy per run of tokens whose rows are adjacent in the
+        // cache (consecutive slots of a page, dense token rows); freqs rows:
+        // one copy per run of consecutive positions when positions are the
+        // slot positions.  Runs cut the number of copies per group from
+        // about 2 x TPB to a few.
+        const int64_t kprev = __shfl_up_sync(0xffffffffu, kbase, 1);
+        const bool kcont = a.rows_contig && lane > 0 && lane < ntok && qok && kbase >= 0 &&
+                           kprev >= 0 && kbase == kprev + a.s_token;
+        const uint32_t kstarts = __ballot_sync(0xffffffffu, lane < ntok && qok && kbase >= 0 && !kcont);
+        const uint64_t pprev = __shfl_up_sync(0xffffffffu, p[0], 1);
+        const uint32_t qok_mask = __ballot_sync(0xffffffffu, lane < ntok && qok);
+        const bool fcont = a.mode == 0 && lane > 0 && lane < ntok && qok &&
+                           ((qok_mask >> (lane - 1)) & 1u) && p[0] == pprev + 1;
+        const uint32_t fstarts = __ballot_sync(0xffffffffu, lane < ntok && qok && !fcont);
         if (lane < ntok && qok) {
-            if (kbase >= 0) {
+            if (kbase >= 0 && !kcont) {
                 unsigned char* kdst = st + a.k_off + (size_t)lane * a.Hk * row_bytes;
-                if (a.heads_contig) {
+                if (a.rows_contig) {
+                    uint32_t n = 1;  // run length: up to the next run start
+                    while (lane + n < ntok && ((kstarts >> (lane + n)) & 1u) == 0u &&
+                           ((qok_mask >> (lane + n)) & 1u) && meta[lane + n].kbase >= 0)
+                        ++n;
+                    bulk_load(kdst, a.cache + kbase, n * a.Hk * row_bytes, &full[s]);
+                } else if (a.heads_contig) {
                     bulk_load(kdst, a.cache + kbase, a.Hk * row_bytes, &full[s]);
                 } else {
                     for (uint32_t h = 0; h < a.Hk; ++h)
@@ -149,11 +173,22 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
                                   row_bytes, &full[s]);
                 }
             }
-            for (uint32_t r = 0; r < a.R; ++r) {
-                const uint32_t lo = a.span_lo[r], hi = a.span_hi[r];
-                if (hi > lo)
-                    bulk_load(st + a.f_off + ((size_t)lane * a.R + r) * a.S * 4u + lo * 8u,
-                              a.freqs + p[r] * a.S + 2u * lo, (hi - lo) * 8u, &full[s]);
+            if (a.mode == 0) {
+                if (!fcont) {
+                    uint32_t n = 1;
+                    while (lane + n < ntok && ((fstarts >> (lane + n)) & 1u) == 0u &&
+                           ((qok_mask >> (lane + n)) & 1u))
+                        ++n;
+                    bulk_load(st + a.f_off + (size_t)lane * a.R * a.S * 4u, a.freqs + p[0] * a.S,
+                              n * a.S * 4u, &full[s]);
+                }
+            } else {
+                for (uint32_t r = 0; r < a.R; ++r) {
+                    const uint32_t lo = a.span_lo[r], hi = a.span_hi[r];
+                    if (hi > lo)
+                        bulk_load(st + a.f_off + ((size_t)lane * a.R + r) * a.S * 4u + lo * 8u,
+                                  a.freqs + p[r] * a.S + 2u * lo, (hi - lo) * 8u, &full[s]);
+                }
             }
         }
     }
@@ -302,6 +337,159 @@ cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------
+// Register-staged variant, used for mrope.  With three position rows per
+// token the pipelined kernel would need three small freqs copies per token,
+// and tiny bulk copies cost more than they save; here the CTA has one thread
+// per 8-pair item of a token (rounded up to warps) and walks TPB tokens:
+// query loads first, then the ragged lookup, then every thread helps gather
+// the tokens' composed (cos, sin) rows into shared memory (one round trip),
+// then key rows are loaded and everything is rotated and stored.
+template <bool INTERLEAVED, int TPB>
+__global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t* s_off = s_dyn;
+    uint32_t* s_clen = s_dyn + a.B + 1;
+    __shared__ __align__(16) float s_cs[TPB][kMaxHead];  // composed (cos, sin) per pair
+    __shared__ int64_t s_kbase[TPB];
+    __shared__ int s_bad[TPB];
+
+    const uint32_t groups = a.S >> 4;  // items per head
+    const uint32_t i = threadIdx.x;
+    const bool has_item = i < a.items;
+    const uint32_t h = has_item ? i / groups : 0u;
+    const uint32_t m = has_item ? i % groups : 0u;
+    const bool is_q = has_item && h < a.Hq;
+    const uint32_t t_begin = blockIdx.x * TPB;
+    // element offsets of the two vectors of this item inside a head row
+    const uint32_t e0 = INTERLEAVED ? 16u * m : 8u * m;
+    const uint32_t e1 = INTERLEAVED ? 16u * m + 8u : (a.S >> 1) + 8u * m;
+
+    if (i < TPB) s_bad[i] = 0;
+
+    // phase 0: query data
+    uint4 xa[TPB], xb[TPB];
+#pragma unroll
+    for (int u = 0; u < TPB; ++u) {
+        xa[u] = make_uint4(0, 0, 0, 0);
+        xb[u] = xa[u];
+        const uint32_t t = t_begin + u;
+        if (is_q && t < a.T) {
+            const uint16_t* row = a.q_in + ((uint64_t)t * a.Hq + h) * a.S;
+            xa[u] = ld_stream(reinterpret_cast<const uint4*>(row + e0));
+            xb[u] = ld_stream(reinterpret_cast<const uint4*>(row + e1));
+        }
+    }
+
+    // phase 1: ragged metadata (contains a __syncthreads, so s_bad is ready)
+    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+
+    // phase 2a: slot row of each token
+    if (i < TPB) {
+        const uint32_t t = t_begin + i;
+        int64_t base = -1;
+        if (t < a.T) {
+            const uint32_t b = find_request(s_off, a.B, t);
+            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+            base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                            a.s_token, a.layer_off, b, pos);
+        }
+        s_kbase[i] = base;
+    }
+    // phase 2b: composed freqs rows, one (cos, sin) pair per rotary pair
+    const uint32_t half = a.S >> 1;
+    for (uint32_t idx = threadIdx.x; idx < TPB * half; idx += blockDim.x) {
+        const uint32_t u = idx / half, k = idx % half;
+        const uint32_t t = t_begin + u;
+        if (t >= a.T) continue;
+        uint64_t p;
+        if (a.mode == 0) {
+            const uint32_t b = find_request(s_off, a.B, t);
+            p = (uint64_t)s_clen[b] + (t - s_off[b]);
+        } else if (a.mode == 1) {
+            p = __ldg(a.position_ids + t);
+        } else {
+            p = __ldg(a.position_ids + (uint64_t)section_of(a, k) * a.T + t);
+        }
+        float2 cs = make_float2(0.f, 0.f);
+        if (p < a.freqs_rows)
+            cs = __ldg(reinterpret_cast<const float2*>(a.freqs + p * a.S) + k);
+        else
+            s_bad[u] = 1;
+        *reinterpret_cast<float2*>(&s_cs[u][2 * k]) = cs;
+    }
+    __syncthreads();
+
+    // phase 3a: key data (needs the slot rows)
+    if (has_item && !is_q) {
+#pragma unroll
+        for (int u = 0; u < TPB; ++u) {
+            const int64_t kb = s_kbase[u];
+            if (kb >= 0 && !s_bad[u]) {
+                const uint16_t* row = a.cache + kb + (int64_t)(h - a.Hq) * a.s_head;
+                xa[u] = *reinterpret_cast<const uint4*>(row + e0);
+                xb[u] = *reinterpret_cast<const uint4*>(row + e1);
+            }
+        }
+    }
+    if (i < TPB && t_begin + i < a.T) {
+        if (s_bad[i])
+            flag(a.err_flags, KVW_ERR_POSITION);
+        else if (s_kbase[i] < 0)
+            flag(a.err_flags, KVW_ERR_PAGE);
+    }
+    if (!has_item) return;
+
+    // phase 3b: rotate and store
+#pragma unroll
+    for (int u = 0; u < TPB; ++u) {
+        const uint32_t t = t_begin + u;
+        if (t >= a.T || s_bad[u]) continue;
+        if (!is_q && s_kbase[u] < 0) continue;
+        const float4* cs4 = reinterpret_cast<const float4*>(&s_cs[u][16u * m]);
+        const float4 c0 = cs4[0], c1 = cs4[1], c2 = cs4[2], c3 = cs4[3];
+        const float c[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
+        const float s[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
+        float va[8], vb[8], ya[8], yb[8];
+        unpack8(xa[u], va);
+        unpack8(xb[u], vb);
+        if (INTERLEAVED) {  // pairs (va0,va1) (va2,va3) .. (vb6,vb7)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                rope_pair(va[2 * q], va[2 * q + 1], c[q], s[q], ya[2 * q], ya[2 * q + 1]);
+                rope_pair(vb[2 * q], vb[2 * q + 1], c[q + 4], s[q + 4], yb[2 * q], yb[2 * q + 1]);
+            }
+        } else {  // pairs (va[q], vb[q])
+#pragma unroll
+            for (int q = 0; q < 8; ++q) rope_pair(va[q], vb[q], c[q], s[q], ya[q], yb[q]);
+        }
+        uint16_t* row = is_q ? a.q_out + ((uint64_t)t * a.Hq + h) * a.S
+                             : a.cache + s_kbase[u] + (int64_t)(h - a.Hq) * a.s_head;
+        if (is_q) {
+            st_stream(reinterpret_cast<uint4*>(row + e0), pack8_bf16(ya));
+            st_stream(reinterpret_cast<uint4*>(row + e1), pack8_bf16(yb));
+        } else {
+            *reinterpret_cast<uint4*>(row + e0) = pack8_bf16(ya);
+            *reinterpret_cast<uint4*>(row + e1) = pack8_bf16(yb);
+        }
+    }
+}
+
+template <bool INTERLEAVED, int TPB>
+cudaError_t launch_staged(const GqaArgs& a, uint32_t threads, size_t smem, cudaStream_t stream) {
+    auto k = qk_rope_staged_kernel<INTERLEAVED, TPB>;
+    if (smem > 16 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const uint32_t blocks = (a.T + TPB - 1) / TPB;
+    k<<<blocks, threads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -388,7 +576,25 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
         a.span_hi[0] = S / 2;
         a.span_lo[1] = a.span_hi[1] = a.span_lo[2] = a.span_hi[2] = 0;
     }
+    a.items = (uint32_t)items;
+    if (a.mode == 2) {
+        const uint32_t threads = (uint32_t)((items + 31) / 32 * 32);
+        const size_t smem_st = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
+        int tpb = 4;
+        while (tpb > 1 && (uint64_t)(tot_seq_len + tpb - 1) / tpb < 152ull * 4) tpb >>= 1;
+        cudaError_t es;
+        if (interleaved)
+            es = tpb == 4 ? launch_staged<true, 4>(a, threads, smem_st, stream)
+               : tpb == 2 ? launch_staged<true, 2>(a, threads, smem_st, stream)
+                          : launch_staged<true, 1>(a, threads, smem_st, stream);
+        else
+            es = tpb == 4 ? launch_staged<false, 4>(a, threads, smem_st, stream)
+               : tpb == 2 ? launch_staged<false, 2>(a, threads, smem_st, stream)
+                          : launch_staged<false, 1>(a, threads, smem_st, stream);
+        return es == cudaSuccess ? KVW_OK : KVW_ECUDA;
+    }
     a.heads_contig = cache->stride_head == (int64_t)S ? 1u : 0u;
+    a.rows_contig = a.heads_contig && cache->stride_token == (int64_t)a.Hk * S ? 1u : 0u;
 
     // shared memory: barriers | ragged tables | kStages x (q | k | freqs | meta)
     const uint32_t tables = (uint32_t)(((2ull * num_batches + 1) * 4 + 127) / 128 * 128);

@@ -40,12 +40,15 @@ struct KnArgs {
     uint32_t tl_log2;         // team size = 1 << tl_log2
     uint32_t nv;              // 16-byte vectors per row = ceil(G / 8)
     uint32_t rows_per_block;
-    uint64_t rows;            // T * rows_per_token
+    uint32_t rows;            // T * rows_per_token
     float eps, wo;
     int mbc;
 };
 
-template <int VPL, int RPT>
+// MBC: multiply_before_cast; FULL: gamma_len is a multiple of 8 (no ragged
+// vector).  Both are template parameters so the per-element inner loops are
+// branch-free: unpack, square-and-add, scale, weight, pack.
+template <int VPL, int RPT, bool MBC, bool FULL>
 __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
@@ -56,29 +59,28 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
     const uint32_t team = threadIdx.x >> a.tl_log2;
     const uint32_t tl = threadIdx.x & (TL - 1u);
     const uint32_t teams = kThreads >> a.tl_log2;
-    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows_per_block;
-    const uint32_t t_lo = (uint32_t)(r0 / a.rows_per_token);
+    const uint32_t r0 = blockIdx.x * a.rows_per_block;
+    const uint32_t t_lo = r0 / a.rows_per_token;
 
     // weights of this lane's columns (the same for every row)
     float w[VPL][8];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
-        const uint32_t vec = tl + v * TL;
-        if (vec < a.nv) {
-            const uint32_t c = vec * 8u;
-            if (c + 8u <= a.G) {
+        const uint32_t c = (tl + v * TL) * 8u;
+        if (FULL) {
+            if (c < a.G) {
                 float g[8];
                 unpack8(ld_table(reinterpret_cast<const uint4*>(a.gamma + c)), g);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) w[v][e] = __fadd_rn(g[e], a.wo);
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w[v][e] = (c + e < a.G) ? __fadd_rn(bf16_lo(a.gamma[c + e]), a.wo) : 0.0f;
+                for (int e = 0; e < 8; ++e) w[v][e] = 0.0f;
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[v][e] = 0.0f;
+            for (int e = 0; e < 8; ++e)
+                w[v][e] = (c + e < a.G) ? __fadd_rn(bf16_lo(a.gamma[c + e]), a.wo) : 0.0f;
         }
     }
 
@@ -86,8 +88,8 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-    const uint64_t r_end = min(r0 + a.rows_per_block, a.rows);
-    const uint32_t t_hi = (uint32_t)((r_end - 1) / a.rows_per_token);
+    const uint32_t r_end = min(r0 + a.rows_per_block, a.rows);
+    const uint32_t t_hi = (r_end - 1) / a.rows_per_token;
     for (uint32_t k = threadIdx.x; k <= t_hi - t_lo; k += kThreads) {
         const uint32_t t = t_lo + k;
         const uint32_t b = find_request(s_off, a.B, t);
@@ -99,33 +101,26 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
     }
     __syncthreads();
 
-    // element offsets of this lane's vectors for each of its rows
-    int64_t addr[RPT][VPL];
-    bool live[RPT];
+    // pointers of this lane's first vector in each of its rows (null: no row)
+    uint16_t* ptr[RPT];
     uint4 x[RPT][VPL];
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
-        const uint64_t r = r0 + team + (uint64_t)q * teams;
-        live[q] = false;
-        int64_t base = -1;
-        uint32_t g = 0;
+        const uint32_t r = r0 + team + q * teams;
+        ptr[q] = nullptr;
         if (r < r_end) {
-            const uint32_t t = (uint32_t)(r / a.rows_per_token);
-            g = (uint32_t)(r % a.rows_per_token);
-            base = s_base[t - t_lo];
-            live[q] = base >= 0;
+            const uint32_t t = r / a.rows_per_token;
+            const uint32_t g = r - t * a.rows_per_token;
+            const int64_t base = s_base[t - t_lo];
+            if (base >= 0) ptr[q] = a.cache + base + (a.per_head ? (int64_t)g * a.s_head : 0);
         }
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-            const uint32_t vec = tl + v * TL;
-            addr[q][v] = -1;
             x[q][v] = make_uint4(0, 0, 0, 0);
-            if (live[q] && vec < a.nv) {
-                const uint32_t c = vec * 8u;  // column inside the normalised row
-                const int64_t off = a.per_head ? (int64_t)g * a.s_head + c
-                                               : (int64_t)(c / a.S) * a.s_head + (c % a.S);
-                addr[q][v] = base + off;
-                x[q][v] = *reinterpret_cast<const uint4*>(a.cache + addr[q][v]);
+            const uint32_t c = (tl + v * TL) * 8u;  // column inside the normalised row
+            if (ptr[q] && c < a.G) {
+                const uint32_t off = a.per_head ? c : (c / a.S) * (uint32_t)a.s_head + (c % a.S);
+                x[q][v] = *reinterpret_cast<const uint4*>(ptr[q] + off);
             }
         }
     }
@@ -140,51 +135,58 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
             const uint32_t c = (tl + v * TL) * 8u;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (c + e < a.G) ss = __fadd_rn(ss, __fmul_rn(xs[v][e], xs[v][e]));
+                if (FULL || c + e < a.G) ss = __fadd_rn(ss, __fmul_rn(xs[v][e], xs[v][e]));
         }
         for (uint32_t o = TL >> 1; o > 0; o >>= 1)
             ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-        if (!live[q]) continue;
-        const float r = rms_inv(ss, (float)a.G, a.eps);
+        if (!ptr[q]) continue;
+        const float rinv = rms_inv(ss, (float)a.G, a.eps);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-            if (addr[q][v] < 0) continue;
             const uint32_t c = (tl + v * TL) * 8u;
+            if (c >= a.G) continue;
             float y[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float xr = __fmul_rn(xs[v][e], r);
-                if (a.mbc) {
-                    y[e] = __fmul_rn(xr, w[v][e]);
-                } else {
-                    const float xr_c = __bfloat162float(__float2bfloat16_rn(xr));
-                    y[e] = __fmul_rn(xr_c, w[v][e]);
-                }
+                const float xr = __fmul_rn(xs[v][e], rinv);
+                y[e] = MBC ? __fmul_rn(xr, w[v][e])
+                           : __fmul_rn(__bfloat162float(__float2bfloat16_rn(xr)), w[v][e]);
             }
             const uint4 out = pack8_bf16(y);
-            if (c + 8u <= a.G) {
-                *reinterpret_cast<uint4*>(a.cache + addr[q][v]) = out;
+            uint16_t* dst =
+                ptr[q] + (a.per_head ? c : (c / a.S) * (uint32_t)a.s_head + (c % a.S));
+            if (FULL || c + 8u <= a.G) {
+                *reinterpret_cast<uint4*>(dst) = out;
             } else {  // ragged tail of the gamma-length slice: columns < G only
                 const uint32_t words[4] = {out.x, out.y, out.z, out.w};
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    if (c + e < a.G)
-                        a.cache[addr[q][v] + e] = (uint16_t)(e & 1 ? words[e >> 1] >> 16 : words[e >> 1]);
+                    if (c + e < a.G) dst[e] = (uint16_t)(e & 1 ? words[e >> 1] >> 16 : words[e >> 1]);
             }
         }
     }
 }
 
-template <int VPL, int RPT>
-cudaError_t launch(const KnArgs& a, size_t smem, cudaStream_t stream) {
-    auto k = rms_norm_kv_kernel<VPL, RPT>;
+template <int VPL, int RPT, bool MBC, bool FULL>
+cudaError_t launch_one(const KnArgs& a, size_t smem, cudaStream_t stream) {
+    auto k = rms_norm_kv_kernel<VPL, RPT, MBC, FULL>;
     if (smem > 32 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const uint64_t blocks = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
-    k<<<(uint32_t)blocks, kThreads, smem, stream>>>(a);
+    const uint32_t blocks = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
+    k<<<blocks, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <int VPL, int RPT>
+cudaError_t launch(const KnArgs& a, size_t smem, cudaStream_t stream) {
+    const bool full = a.G % 8 == 0;
+    if (a.mbc)
+        return full ? launch_one<VPL, RPT, true, true>(a, smem, stream)
+                    : launch_one<VPL, RPT, true, false>(a, smem, stream);
+    return full ? launch_one<VPL, RPT, false, true>(a, smem, stream)
+                : launch_one<VPL, RPT, false, false>(a, smem, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -246,7 +248,9 @@ extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const
     a.tl_log2 = 0;
     while ((1u << a.tl_log2) < tl) ++a.tl_log2;
     const uint32_t vpl = (a.nv + tl - 1) / tl;
-    a.rows = (uint64_t)total_seq_len * a.rows_per_token;
+    const uint64_t rows = (uint64_t)total_seq_len * a.rows_per_token;
+    if (rows > 0xfffff000ull) return KVW_EUNSUPPORTED;
+    a.rows = (uint32_t)rows;
     a.eps = epsilon;
     a.wo = weight_offset;
     a.mbc = multiply_before_cast ? 1 : 0;
