@@ -51,6 +51,21 @@ def kind(name):
     return name[:3]
 
 
+def combine_ranks(ms, tokens, world, device=None):
+    """Replicas: the job's time is the slowest rank's, its work the sum of the
+    ranks' tokens.  Only timing crosses ranks; there is no data collective."""
+    if world == 1:
+        return ms, tokens
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
@@ -297,11 +312,7 @@ def run_ours(args):
     clk = clocks.stop()
     per = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(per)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    tokens_all = w.T * world
+    ms_max, tokens_all = combine_ranks(ms, w.T, world, dev)
     value = tokens_all / (ms_max / 1000.0)
     assert d.flags() == 0, "kernel reported data errors on the benchmark inputs"
 
@@ -310,13 +321,13 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(d, w, k, stream, dev, max(3, min(args.steps, 200)), args.warmup)
-        if world > 1:
-            t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["ms"] = float(t.item())
+        e2e["ms"], _ = combine_ranks(e2e["ms"], w.T, world, dev)
         e2e = {"value": tokens_all / (e2e["ms"] / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-               "ms_per_step": e2e["ms"]}
+               "ms_per_step": e2e["ms"],
+               "how": "pinned host inputs -> device, kvw call, results -> pinned host, every "
+                      "step; steps pipelined %d deep on copy-in / compute / copy-out streams, "
+                      "8 steps per CUDA graph replay" % e2e["depth"]}
 
     peak, peak_src = measured_peak()
     achieved = abytes / (ms / 1000.0) / 1e9
@@ -353,49 +364,118 @@ def run_ours(args):
     return 0
 
 
-def measure_e2e(d, w, k, stream, dev, steps, warmup):
-    """Host buffers in and out, copies inside the timed region."""
+def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=2):
+    """Throughput through the public API with host buffers: every step copies
+    its inputs from pinned host memory, launches the entry point and copies
+    its results back.  Steps are pipelined ``depth`` deep over separate
+    copy-in, compute and copy-out streams (a serving loop overlaps step i's
+    compute with step i+1's inputs and step i-1's results), each buffer set
+    reused only after the step that last used it is done."""
+    import ctypes
+
     import torch
 
-    from gqa_kv_cache_mla_gb300 import device as D
+    from gqa_kv_cache_mla_gb300 import kvw
 
     def pinned(t):
         return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
 
-    if k == "mla":
-        ins = [d.q.tensor, d.kv.tensor, d.offsets.tensor, d.cache_lengths.tensor,
-               d.page_table.tensor]
-        outs = [d.q_out.tensor, d.err.tensor]
-    elif k == "gqa":
-        ins = [d.q.tensor, d.offsets.tensor, d.cache_lengths.tensor, d.page_table.tensor]
-        if d.pos is not None:
-            ins.append(d.pos.tensor)
-        outs = [d.out.tensor, d.err.tensor]
-    else:
-        ins = [d.offsets.tensor, d.cache_lengths.tensor, d.page_table.tensor]
-        outs = [d.err.tensor]
-    h_in = [pinned(t) for t in ins]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    sets = []
+    for i in range(depth):
+        if k == "mla":
+            ins = {"q": d.q.tensor, "kv": d.kv.tensor, "off": d.offsets.tensor,
+                   "clen": d.cache_lengths.tensor, "pt": d.page_table.tensor}
+            outs = {"q_out": d.q_out.tensor, "err": d.err.tensor}
+        elif k == "gqa":
+            ins = {"q": d.q.tensor, "off": d.offsets.tensor, "clen": d.cache_lengths.tensor,
+                   "pt": d.page_table.tensor}
+            if d.pos is not None:
+                ins["pos"] = d.pos.tensor
+            outs = {"out": d.out.tensor, "err": d.err.tensor}
+        else:
+            ins = {"off": d.offsets.tensor, "clen": d.cache_lengths.tensor,
+                   "pt": d.page_table.tensor}
+            outs = {"err": d.err.tensor}
+        h_in = {n: pinned(t) for n, t in ins.items()}  # the step's inputs, on the host
+        if i > 0:  # its own device buffers
+            ins = {n: torch.empty_like(t) for n, t in ins.items()}
+            outs = {n: torch.empty_like(t) for n, t in outs.items()}
+        desc = kvw.PagedCacheT()
+        ctypes.memmove(ctypes.byref(desc), ctypes.byref(d.desc), ctypes.sizeof(desc))
+        desc.page_table = ins["pt"].data_ptr()
+        desc.cache_lengths = ins["clen"].data_ptr()
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+        sets.append(dict(ins=ins, outs=outs, desc=desc, h_in=h_in, h_out=h_out,
+                         computed=torch.cuda.Event(), copied_out=torch.cuda.Event()))
+    h2d = sum(t.numel() * t.element_size() for t in sets[0]["h_in"].values())
+    d2h = sum(t.numel() * t.element_size() for t in sets[0]["h_out"].values())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def step():
-        for dst, src in zip(ins, h_in):
-            dst.copy_(src, non_blocking=True)
-        d.run(stream=stream)
-        for dst, src in zip(h_out, outs):
-            dst.copy_(src, non_blocking=True)
+    def call(S, stream):
+        i, o = S["ins"], S["outs"]
+        if k == "mla":
+            kvw.kvw_mla_rope_rmsnorm_quant(o["q_out"], i["q"], i["off"], d.freqs.tensor,
+                                           d.gamma.tensor, i["kv"], S["desc"], w.layer_idx,
+                                           w.epsilon, o["err"], stream,
+                                           kv_row_stride=w.kv_in.shape[-1])
+        elif k == "gqa":
+            kvw.kvw_qk_rope_paged_ragged(
+                i["q"], i["off"], S["desc"], d.freqs.tensor, i.get("pos"), w.interleaved,
+                None if w.mrope_section is None else [int(v) for v in w.mrope_section],
+                w.layer_idx, o["out"], o["err"], stream)
+        else:
+            kvw.kvw_rms_norm_kv_cache_paged(S["desc"], d.gamma.tensor, w.epsilon,
+                                            w.weight_offset, w.layer_idx, w.T, i["off"],
+                                            w.multiply_before_cast, True, o["err"], stream)
 
-    for _ in range(warmup):
-        step()
+    def step(n, S, comp, first):
+        in_ready = torch.cuda.Event()
+        s_in.wait_stream(comp) if first else s_in.wait_event(S["computed"])
+        with torch.cuda.stream(s_in):
+            for name, t in S["ins"].items():
+                t.copy_(S["h_in"][name], non_blocking=True)
+            in_ready.record(s_in)
+        comp.wait_event(in_ready)
+        if not first:
+            comp.wait_event(S["copied_out"])  # its outputs were read back
+        with torch.cuda.stream(comp):
+            S["outs"]["err"].zero_()
+            call(S, comp)
+            S["computed"].record(comp)
+        s_out.wait_event(S["computed"])
+        with torch.cuda.stream(s_out):
+            for name, t in S["outs"].items():
+                S["h_out"][name].copy_(t, non_blocking=True)
+            S["copied_out"].record(s_out)
+
+    # K steps per CUDA graph: the copy-in / compute / copy-out streams overlap
+    # inside the graph and one graph launch replaces ~13 host calls per step
+    K = 4 * depth
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+        for n in range(K):
+            step(n, sets[n % depth], cap, first=n < depth)
+        s_in_done, s_out_done = torch.cuda.Event(), torch.cuda.Event()
+        s_in_done.record(s_in)
+        s_out_done.record(s_out)
+        cap.wait_event(s_in_done)
+        cap.wait_event(s_out_done)
+    reps = max(1, (steps + K - 1) // K)
+    for _ in range(max(1, warmup // K)):
+        graph.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    launch = torch.cuda.current_stream(dev)
+    a.record(launch)
+    for _ in range(reps):
+        graph.replay()
+    b.record(launch)
     torch.cuda.synchronize()
-    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h}
+    for S in sets:
+        assert int(S["h_out"]["err"][0]) == 0, "data errors in the e2e run"
+    steps = reps * K
+    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h, "depth": depth}
 
 
 def main():
