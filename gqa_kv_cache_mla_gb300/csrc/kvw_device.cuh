@@ -187,11 +187,13 @@ __device__ __forceinline__ int64_t slot_row(const uint32_t* __restrict__ page_ta
                                            uint32_t max_pages, uint32_t num_pages,
                                            uint32_t page_size, int64_t s_page, int64_t s_token,
                                            int64_t layer_off, uint32_t b, uint64_t pos) {
-    const uint64_t pidx = pos / page_size;
+    if (pos >> 32) return -1;  // no page table reaches that far (max_pages is 32-bit)
+    const uint32_t p32 = (uint32_t)pos;
+    const uint32_t pidx = p32 / page_size, row = p32 - pidx * page_size;
     if (pidx >= max_pages) return -1;
     const uint32_t page = __ldg(page_table + (uint64_t)b * max_pages + pidx);
     if (page >= num_pages) return -1;
-    return (int64_t)page * s_page + layer_off + (int64_t)(pos % page_size) * s_token;
+    return (int64_t)page * s_page + layer_off + (int64_t)row * s_token;
 }
 
 // ------------------------------------------------------------ TMA + mbarrier

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
     uint32_t* s_clen = s_dyn + a.B + 1;
-    __shared__ int64_t s_base[kThreads * RPT / 4 + 2];
+    __shared__ int64_t s_base[kThreads * 2 + 2];  // tokens of up to 512 rows
 
     const uint32_t TL = 1u << a.tl_log2;
     const uint32_t team = threadIdx.x >> a.tl_log2;
@@ -101,18 +101,26 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
     }
     __syncthreads();
 
-    // pointers of this lane's first vector in each of its rows (null: no row)
+    // pointers of this lane's first vector in each of its rows (null: no row);
+    // row r = r0 + team + q * teams, walked as (token, head) without dividing
     uint16_t* ptr[RPT];
     uint4 x[RPT][VPL];
+    uint32_t t = (r0 + team) / a.rows_per_token;
+    uint32_t g = (r0 + team) - t * a.rows_per_token;
+    const uint32_t dt = teams / a.rows_per_token, dg = teams - dt * a.rows_per_token;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
         const uint32_t r = r0 + team + q * teams;
         ptr[q] = nullptr;
         if (r < r_end) {
-            const uint32_t t = r / a.rows_per_token;
-            const uint32_t g = r - t * a.rows_per_token;
             const int64_t base = s_base[t - t_lo];
             if (base >= 0) ptr[q] = a.cache + base + (a.per_head ? (int64_t)g * a.s_head : 0);
+        }
+        t += dt;
+        g += dg;
+        if (g >= a.rows_per_token) {
+            g -= a.rows_per_token;
+            ++t;
         }
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
@@ -243,8 +251,12 @@ extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const
     a.per_head = per_head_norm ? 1u : 0u;
     a.rows_per_token = per_head_norm ? cache->num_heads : 1u;
     a.nv = (gamma_len + 7) / 8;
+    // Team of TL lanes per row, each lane VPL 16-byte vectors: narrow teams
+    // (4 lanes for up to 16 vectors) let one instruction stream serve many
+    // rows, so the per-row work (shuffles, the reciprocal square root,
+    // addressing) is shared by more rows per warp.
     uint32_t tl = 4;
-    while (tl < a.nv && tl < 32) tl <<= 1;
+    while (tl < 32 && tl * 4 < a.nv) tl <<= 1;
     a.tl_log2 = 0;
     while ((1u << a.tl_log2) < tl) ++a.tl_log2;
     const uint32_t vpl = (a.nv + tl - 1) / tl;
@@ -258,14 +270,14 @@ extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const
     const uint32_t teams = kThreads / tl;
     cudaError_t e;
     if (vpl <= 1) {
-        a.rows_per_block = teams * 4;
-        e = launch<1, 4>(a, smem, stream);
+        a.rows_per_block = teams * 8;
+        e = launch<1, 8>(a, smem, stream);
     } else if (vpl <= 2) {
-        a.rows_per_block = teams * 2;
-        e = launch<2, 2>(a, smem, stream);
+        a.rows_per_block = teams * 4;
+        e = launch<2, 4>(a, smem, stream);
     } else if (vpl <= 4) {
-        a.rows_per_block = teams;
-        e = launch<4, 1>(a, smem, stream);
+        a.rows_per_block = teams * 2;
+        e = launch<4, 2>(a, smem, stream);
     } else {
         a.rows_per_block = teams;
         e = launch<8, 1>(a, smem, stream);
