@@ -90,12 +90,15 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
     for (uint32_t g = blockIdx.x; g < a.groups; g += gridDim.x, ++it) {
         const uint32_t s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
-        if (it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+        // With position_ids the slot resolution takes two dependent loads
+        // (position, then page); resolving before waiting for the stage hides
+        // them under the consumers' work.  With slot positions (one load) the
+        // wait comes first: that order measured faster there.
+        const bool early = a.mode != 0;
+        if (!early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
             if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
             break;
         }
-        unsigned char* st = stages + (size_t)s * a.stage_bytes;
-        TokMeta* meta = reinterpret_cast<TokMeta*>(st + a.meta_off);
         const uint32_t t0 = g * a.tpb;
         const uint32_t ntok = min(a.tpb, a.T - t0);
         uint64_t p[3] = {0, 0, 0};
@@ -130,6 +133,14 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
                 for (uint32_t r = 0; r < a.R; ++r) bytes += (a.span_hi[r] - a.span_lo[r]) * 8u;
                 if (kbase >= 0) bytes += a.Hk * row_bytes;
             }
+        }
+        if (early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+            if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
+            break;
+        }
+        unsigned char* st = stages + (size_t)s * a.stage_bytes;
+        TokMeta* meta = reinterpret_cast<TokMeta*>(st + a.meta_off);
+        if (lane < ntok) {
             meta[lane].kbase = kbase;
             meta[lane].qok = qok;
         }

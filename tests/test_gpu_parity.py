@@ -338,3 +338,23 @@ def test_mla_stream_path_flags(orc, dev):
     w.cache.page_table[1, 3] = W.PAGE_UNMAPPED
     d, _, _ = run_mla(orc, dev, w)
     assert d.flags() == 3
+
+
+# ------------------------------------------------------------ maximum request count
+
+def test_max_batches_all_entry_points(orc, dev):
+    """num_batches = 8192 (the documented maximum): the staged ragged tables
+    take 64 KiB of shared memory in every kernel."""
+    rng = np.random.default_rng(901)
+    B = 8192
+    new = rng.integers(0, 3, B)
+    prior = rng.integers(0, 100, B)
+    w = W.mla_workload("mb", 902, new, prior, num_heads=4, page_size=32, max_seq_len=128,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    assert w.B == B
+    run_mla(orc, dev, w)
+    g = W.gqa_workload("mb", 903, new, prior, 4, 2, 64, page_size=32, freqs_rows=128,
+                       base=10000.0, interleaved=True, position_mode="ids")
+    run_gqa(orc, dev, g)
+    k = W.knorm_workload("mb", 904, new, prior, 2, 64, page_size=32, gamma_len=64)
+    run_knorm(orc, dev, k)
