@@ -114,7 +114,8 @@ def algorithmic_bytes(w, name):
             rows = len(np.unique(np.concatenate(
                 [c.cache_lengths[b] + np.arange(w.offsets[b + 1] - w.offsets[b])
                  for b in range(w.B)])))
-            return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, rows)
+            return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, rows,
+                                           c.elem_bytes)
         # mrope / ids: each distinct (row, pair-range) read counts; bound by distinct rows
         rows = len(np.unique(w.position_ids))
         per_row = c.head_size * 4

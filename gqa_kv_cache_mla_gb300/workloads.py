@@ -50,6 +50,14 @@ def bf16_bits(x) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def e4m3_bits(x) -> np.ndarray:
+    """Round fp32 values to FP8 E4M3FN (library cast) and return the codes."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
 def rope_table(rows: int, dim: int, base: float) -> np.ndarray:
     """Precomputed freqs_cis table, fp32 ``[rows, dim]``.
 
@@ -205,13 +213,18 @@ def normal_bf16(rng, shape, mean=0.0, std=1.0, outlier_frac=0.0, outlier_mult=20
 
 
 def fill_new_k_rows(rng, cache: PagedCache, offsets, layer_idx):
-    """Overwrite the K rows of new slots with N(0,1) bf16 (stand-in for a QKV GEMM)."""
+    """Overwrite the K rows of new slots with N(0,1) values (stand-in for a
+    QKV GEMM): bf16, or E4M3 codes of N(0,1)/scale for an FP8 cache."""
     v = cache.view6()
     P = cache.page_size
     for t, b, pos in new_slots(offsets, cache.cache_lengths):
         page = int(cache.page_table[b, pos // P])
-        v[page, 0, layer_idx, pos % P, :, :] = normal_bf16(
-            rng, (cache.num_heads, cache.head_size))
+        shape = (cache.num_heads, cache.head_size)
+        if cache.dtype == DTYPE_BF16:
+            v[page, 0, layer_idx, pos % P, :, :] = normal_bf16(rng, shape)
+        else:
+            x = rng.standard_normal(size=shape, dtype=np.float32) / np.float32(cache.scale)
+            v[page, 0, layer_idx, pos % P, :, :] = e4m3_bits(x)
 
 
 @dataclasses.dataclass
@@ -308,7 +321,7 @@ class GQAWorkload:
 def gqa_workload(name, seed, new_lens, prior_lens, num_q_heads, num_kv_heads, head_size,
                  page_size, freqs_rows, base, interleaved, position_mode=None,
                  mrope_section=None, num_layers=2, layer_idx=1, spare_pages=0,
-                 pos_limit=None) -> GQAWorkload:
+                 pos_limit=None, cache_dtype=DTYPE_BF16, scale=1.0) -> GQAWorkload:
     """position_mode: None (slot positions), "ids" ([T]) or "mrope" ([3, T])."""
     rng = rng_for(seed)
     new_lens = np.asarray(new_lens, dtype=np.int64)
@@ -319,7 +332,7 @@ def gqa_workload(name, seed, new_lens, prior_lens, num_q_heads, num_kv_heads, he
     max_pages = int(max(1, (int(total.max()) + page_size - 1) // page_size)) if len(total) else 1
     table, num_pages = build_page_table(rng, total, page_size, max_pages,
                                         spare_pages=spare_pages)
-    cache = make_cache(rng, DTYPE_BF16, 1.0, table, prior_lens, num_pages, 2, num_layers,
+    cache = make_cache(rng, cache_dtype, scale, table, prior_lens, num_pages, 2, num_layers,
                        page_size, num_kv_heads, head_size)
     fill_new_k_rows(rng, cache, offsets, layer_idx)
     q = normal_bf16(rng, (T, num_q_heads, head_size))
@@ -336,14 +349,16 @@ def gqa_workload(name, seed, new_lens, prior_lens, num_q_heads, num_kv_heads, he
                        layer_idx)
 
 
-def gqa_llama3(interleaved=True, position_mode=None, seed=4, num_requests=32) -> GQAWorkload:
+def gqa_llama3(interleaved=True, position_mode=None, seed=4, num_requests=32,
+               cache_dtype=DTYPE_BF16, scale=1.0) -> GQAWorkload:
     """Llama-3-8B: 32 q / 8 kv heads, head 128, new U[1,2048], prior U[0,4096], page 128."""
     rng = rng_for(seed + 1000)
     new = rng.integers(1, 2048, size=num_requests, endpoint=True)
     prior = rng.integers(0, 4096, size=num_requests, endpoint=True)
     sec = (16, 24, 24) if position_mode == "mrope" else None
     return gqa_workload("gqa_llama3", seed, new, prior, 32, 8, 128, 128, 8192, 500000.0,
-                        interleaved, position_mode=position_mode, mrope_section=sec)
+                        interleaved, position_mode=position_mode, mrope_section=sec,
+                        cache_dtype=cache_dtype, scale=scale)
 
 
 @dataclasses.dataclass
@@ -402,8 +417,8 @@ def algorithmic_bytes_mla(T, H, cache_dtype, distinct_positions=None):
     return T * (2 * H * MLA_ROPE_DIM * 2 + MLA_ROW * 2 + MLA_ROW * c) + rows * MLA_ROPE_DIM * 4
 
 
-def algorithmic_bytes_gqa(T, Hq, Hk, S, distinct_rows):
-    return T * (2 * Hq * S * 2 + 2 * Hk * S * 2) + distinct_rows * S * 4
+def algorithmic_bytes_gqa(T, Hq, Hk, S, distinct_rows, k_bytes=2):
+    return T * (2 * Hq * S * 2 + 2 * Hk * S * k_bytes) + distinct_rows * S * 4
 
 
 def algorithmic_bytes_knorm(T, Hk, G):
@@ -435,6 +450,9 @@ REGISTRY = {
                      "GQA Llama-3-8B Q/K RoPE, half-split, position_ids"),
     "gqa_mrope": (lambda s: gqa_llama3(False, "mrope", seed=s + 2), "qk_rope_paged_ragged.cu",
                   "GQA Llama-3-8B Q/K RoPE, half-split, mrope (16,24,24)"),
+    "gqa_fp8k": (lambda s: gqa_llama3(True, None, seed=s + 2, cache_dtype=DTYPE_FP8_E4M3),
+                 "qk_rope_paged_ragged.cu",
+                 "GQA Llama-3-8B Q/K RoPE, interleaved, FP8 E4M3 K cache (scale 1.0)"),
     "knorm128": (lambda s: knorm_paged(128, seed=s + 3), "rms_norm_kv_cache_paged.cu",
                  "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, G=128"),
     "knorm64": (lambda s: knorm_paged(64, seed=s + 3), "rms_norm_kv_cache_paged.cu",

@@ -62,8 +62,8 @@ def _load(path):
         u32, u32, u32, u32, u32, i64, i64, i64, i64, i64, u32, f32, i32]
     L.oracle_qk_rope_paged_ragged.restype = u32
     L.oracle_qk_rope_paged_ragged.argtypes = [
-        vp, vp, u32, u32, u32, vp, vp, u32, vp, u32, u32, u32, u32, u32, i64, i64, i64,
-        i64, i64, vp, u32, vp, i32, vp, u32, vp, i32]
+        vp, vp, u32, u32, u32, vp, i32, f32, vp, u32, vp, u32, u32, u32, u32, u32, i64, i64,
+        i64, i64, i64, vp, u32, vp, i32, vp, u32, vp, i32]
     L.oracle_rms_norm_kv_cache_paged.restype = u32
     L.oracle_rms_norm_kv_cache_paged.argtypes = [
         vp, vp, u32, vp, u32, u32, u32, u32, u32, i64, i64, i64, i64, i64, vp, u32, f32,
@@ -221,7 +221,8 @@ def qk_rope_paged_ragged(w, output=None, cache_data=None, nthreads=1, T=None):
     sec = None if w.mrope_section is None else _c(w.mrope_section, np.uint32)
     s = c.strides
     flags = lib().oracle_qk_rope_paged_ragged(
-        _p(q), _p(off), len(off) - 1, T, q.shape[1], _p(cache_data), _p(c.page_table),
+        _p(q), _p(off), len(off) - 1, T, q.shape[1], _p(cache_data), c.dtype, c.scale,
+        _p(c.page_table),
         c.max_pages_per_seq, _p(c.cache_lengths), c.num_pages, c.num_layers, c.page_size,
         c.num_heads, c.head_size, s[0], s[1], s[2], s[3], s[4], _p(fr), fr.shape[0],
         _p(pid), int(w.interleaved), _p(sec), w.layer_idx, _p(output), nthreads)

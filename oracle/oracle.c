@@ -376,14 +376,38 @@ static void rotate_head_bf16(const uint16_t* x, uint16_t* y, uint32_t S, int int
     memcpy(y, out, sizeof(uint16_t) * S); /* safe when y == x */
 }
 
+/* The same rotation on an FP8 E4M3 head row stored with a per-tensor scale:
+ * each value is dequantised (code value times scale, rounded to fp32),
+ * rotated, and re-encoded as satfinite_rne(y / scale). */
+static void rotate_head_e4m3(uint8_t* x, uint32_t S, int interleaved, float scale,
+                             const float* freqs, uint64_t pos_s, const uint32_t* position_ids,
+                             const uint32_t* sec, uint32_t T, int64_t t) {
+    uint8_t out[1024];
+    for (uint32_t k = 0; k < S / 2; ++k) {
+        uint32_t e0, e1;
+        pair_elems(interleaved, S, k, &e0, &e1);
+        uint64_t p = pair_position(pos_s, position_ids, sec, T, t, k);
+        const float* cs = freqs + p * S;
+        float x0 = oracle_e4m3_to_f32(x[e0]) * scale;
+        float x1 = oracle_e4m3_to_f32(x[e1]) * scale;
+        float y0, y1;
+        rope_pair(x0, x1, cs[2 * k], cs[2 * k + 1], &y0, &y1);
+        out[e0] = oracle_f32_to_e4m3(y0 / scale);
+        out[e1] = oracle_f32_to_e4m3(y1 / scale);
+    }
+    memcpy(x, out, S);
+}
+
 /*
  * generic_fused_qk_rope_bshd_paged_ragged: for every new token t, Q heads
  * q_proj[t, h, :] are rotated into output[t, h, :]; the K rows of the token's
- * slot (all kv heads, layer layer_idx) are rotated in place in the cache.
+ * slot (all kv heads, layer layer_idx) are rotated in place in the cache
+ * (bf16, or FP8 E4M3 with a per-tensor scale: the collection's scale_dtype_ /
+ * quantization_granularity_ parameters).
  */
 uint32_t oracle_qk_rope_paged_ragged(
     const uint16_t* q_proj, const uint32_t* offsets, uint32_t B, uint32_t T, uint32_t Hq,
-    uint16_t* cache, const uint32_t* page_table, uint32_t max_pages,
+    void* cache, int cache_dtype, float scale, const uint32_t* page_table, uint32_t max_pages,
     const uint32_t* cache_lengths, uint32_t num_pages, uint32_t num_layers, uint32_t page_size,
     uint32_t num_kv_heads, uint32_t head_size, int64_t s_page, int64_t s_kv, int64_t s_layer,
     int64_t s_token, int64_t s_head, const float* freqs, uint32_t freqs_rows,
@@ -418,9 +442,16 @@ uint32_t oracle_qk_rope_paged_ragged(
         int64_t base = slot_base(&L, b, pos_s, layer_idx, &f);
         flags |= f;
         if (base < 0) continue;
-        for (uint32_t g = 0; g < num_kv_heads; ++g) {
-            uint16_t* k = cache + base + (int64_t)g * s_head; /* kv index 0 = K */
-            rotate_head_bf16(k, k, S, interleaved, freqs, pos_s, position_ids, mrope_section, T, t);
+        for (uint32_t g = 0; g < num_kv_heads; ++g) { /* kv index 0 = K */
+            if (cache_dtype == ORC_BF16) {
+                uint16_t* k = (uint16_t*)cache + base + (int64_t)g * s_head;
+                rotate_head_bf16(k, k, S, interleaved, freqs, pos_s, position_ids, mrope_section, T,
+                                 t);
+            } else {
+                uint8_t* k = (uint8_t*)cache + base + (int64_t)g * s_head;
+                rotate_head_e4m3(k, S, interleaved, scale, freqs, pos_s, position_ids,
+                                 mrope_section, T, t);
+            }
         }
     }
     free(tok_b);

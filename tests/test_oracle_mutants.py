@@ -34,8 +34,12 @@ MUTANTS = [
     ("row inside page", "uint64_t row = pos % L->page_size;",
      "uint64_t row = (pos + 1) % L->page_size;"),
     ("layer offset dropped", "(int64_t)layer * L->s_layer", "(int64_t)0 * L->s_layer"),
-    ("K rows taken from V", "uint16_t* k = cache + base + (int64_t)g * s_head;",
-     "uint16_t* k = cache + base + s_kv + (int64_t)g * s_head;"),
+    ("K rows taken from V", "uint16_t* k = (uint16_t*)cache + base + (int64_t)g * s_head;",
+     "uint16_t* k = (uint16_t*)cache + base + s_kv + (int64_t)g * s_head;"),
+    ("fp8 K dequantised without the scale", "float x0 = oracle_e4m3_to_f32(x[e0]) * scale;",
+     "float x0 = oracle_e4m3_to_f32(x[e0]);"),
+    ("fp8 K re-quantised without the scale", "out[e1] = oracle_f32_to_e4m3(y1 / scale);",
+     "out[e1] = oracle_f32_to_e4m3(y1);"),
     ("q head order", "uint16_t* yq = q_rope_out + ((int64_t)t * H + h) * ROPE;",
      "uint16_t* yq = q_rope_out + ((int64_t)t * H + (H - 1 - h)) * ROPE;"),
     ("bf16 truncates", "keep += 1u;", "keep += 0u;"),
@@ -70,6 +74,9 @@ PINS = [
     (S.test_position_past_table_skips_token, {}),
     (S.test_unmapped_page_skips_cache_row_only, {}),
     (S.test_fp8_scale_convention, {}),
+    (R.test_gqa_fp8_k_position_zero_is_identity, {}),
+    (R.test_gqa_fp8_k_vs_complex_fp64, {"interleaved": False}),
+    (R.test_gqa_fp8_k_scale_convention, {}),
 ] + [(R.test_gqa_q_and_k_vs_complex_fp64, {"interleaved": i, "mode": m})
      for i in (True, False) for m in (None, "ids", "mrope")]
 

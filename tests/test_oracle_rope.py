@@ -228,3 +228,55 @@ def test_gqa_mrope_single_section_uses_row0(orc):
     b = orc.qk_rope_paged_ragged(w_m)
     assert a[2] == b[2] == 0
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------- GQA with an FP8 K cache
+
+def _gqa_fp8(interleaved=True, mode=None, sec=None, scale=1.0, prior=(0, 7, 20), seed=141):
+    return W.gqa_workload("f8", seed, [3, 5, 2], list(prior), num_q_heads=2, num_kv_heads=2,
+                          head_size=32, page_size=16, freqs_rows=64, base=10000.0,
+                          interleaved=interleaved, position_mode=mode, mrope_section=sec,
+                          cache_dtype=W.DTYPE_FP8_E4M3, scale=scale)
+
+
+def test_gqa_fp8_k_position_zero_is_identity(orc):
+    w = _gqa_fp8(prior=(0, 0, 0), seed=142)
+    w.offsets = np.array([0, 1, 2, 3], np.uint32)  # one token per request: position 0
+    w.q_proj = w.q_proj[:3].copy()
+    _, cache, flags = orc.qk_rope_paged_ragged(w, T=3)
+    assert flags == 0
+    assert np.array_equal(cache, w.cache.data)
+
+
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_gqa_fp8_k_vs_complex_fp64(orc, interleaved):
+    from helpers import expected_slots
+
+    S = 32
+    w = _gqa_fp8(interleaved)
+    out, cache, flags = orc.qk_rope_paged_ragged(w)
+    assert flags == 0
+    c = w.cache
+    theta = _theta(S, 10000.0)
+    before, after = c.view6(), c.view6(cache)
+    dec = orc.e4m3_decode
+    for t, page, row, pos in expected_slots(w.offsets, c.cache_lengths, c.page_table, c.page_size):
+        x = dec(before[page, 0, w.layer_idx, row]).astype(np.float64)
+        y = dec(after[page, 0, w.layer_idx, row]).astype(np.float64)
+        a0, a1 = _pairs(x, interleaved, S)
+        b0, b1 = _pairs(y, interleaved, S)
+        e0, e1 = _exact_rotation(a0, a1, np.broadcast_to(pos * theta, a0.shape))
+        # one E4M3 rounding: half a step of 2^-3 relative, or 2^-10 absolute (subnormals)
+        for b, e in ((b0, e0), (b1, e1)):
+            assert np.all(np.abs(b - e) <= np.abs(e) * 2.0**-4 + 2.0**-9 + 1e-6)
+
+
+def test_gqa_fp8_k_scale_convention(orc):
+    """dequantise with the scale, rotate, re-quantise with it: scale 2 on the
+    same codes gives the same codes (x2 and /2 are exact)."""
+    a = _gqa_fp8(scale=1.0, seed=143)
+    b = _gqa_fp8(scale=1.0, seed=143)
+    b.cache.scale = 2.0
+    _, ca, fa = orc.qk_rope_paged_ragged(a)
+    _, cb, fb = orc.qk_rope_paged_ragged(b)
+    assert fa == fb == 0 and np.array_equal(ca, cb)
