@@ -68,6 +68,50 @@ __device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8]) {
     return v;
 }
 
+// Eight E4M3 codes (little-endian in a uint2) -> fp32, exact (E4M3 values
+// are a subset of fp16, converted with cvt.f16x2.e4m3x2).
+__device__ __forceinline__ void unpack8_e4m3(const uint2& v, float (&f)[8]) {
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_fp8x2_storage_t pair =
+            static_cast<__nv_fp8x2_storage_t>((w[i >> 1] >> (16 * (i & 1))) & 0xffffu);
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+        const float2 x = __half22float2(__half2(h));
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+    }
+}
+
+// Eight key-cache elements at byte address p as fp32: bf16 widened exactly,
+// or E4M3 decoded and multiplied by the per-tensor scale.
+template <bool FP8>
+__device__ __forceinline__ void load_k8(const unsigned char* p, float (&f)[8], float scale) {
+    if constexpr (FP8) {
+        unpack8_e4m3(*reinterpret_cast<const uint2*>(p), f);
+        if (scale != 1.0f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], scale);
+        }
+    } else {
+        unpack8(*reinterpret_cast<const uint4*>(p), f);
+    }
+}
+
+// Eight fp32 values stored as key-cache elements: bf16 round to nearest
+// even, or E4M3 satfinite(y / scale).
+template <bool FP8>
+__device__ __forceinline__ void store_k8(unsigned char* p, const float (&y)[8], float scale) {
+    if constexpr (FP8) {
+        float z[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) z[i] = scale == 1.0f ? y[i] : __fdiv_rn(y[i], scale);
+        *reinterpret_cast<uint2*>(p) = pack8_e4m3(z);
+    } else {
+        *reinterpret_cast<uint4*>(p) = pack8_bf16(y);
+    }
+}
+
 // ------------------------------------------------------------ arithmetic
 
 // Rotation of one pair by (c, s) = (cos, sin): y0 = x0*c - x1*s,

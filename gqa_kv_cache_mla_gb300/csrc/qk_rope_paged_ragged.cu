@@ -33,6 +33,7 @@
 // Rotation arithmetic: fp32, separately rounded products, one rounding to
 // bf16.
 #include <cstdint>
+#include <type_traits>
 
 #include "kvw_device.cuh"
 
@@ -49,7 +50,9 @@ constexpr uint32_t kMaxTPB = 16;
 struct GqaArgs {
     const uint16_t* q_in;  // bf16 [T, Hq, S]
     uint16_t* q_out;       // bf16 [T, Hq, S], may alias q_in
-    uint16_t* cache;       // bf16
+    unsigned char* cache;  // K/V cache bytes (bf16, or FP8 E4M3 with kscale)
+    float kscale;          // FP8 dequantisation scale
+    uint32_t kesz;         // bytes per cache element
     const uint32_t* offsets;
     const uint32_t* cache_lengths;
     const uint32_t* page_table;
@@ -85,7 +88,8 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
                                          const uint32_t* s_off, const uint32_t* s_clen,
                                          unsigned char* stages) {
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t row_bytes = a.S * 2u;
+    const uint32_t row_bytes = a.S * 2u;       // a query row
+    const uint32_t krow_bytes = a.S * a.kesz;  // a key row
     uint32_t it = 0;
     for (uint32_t g = blockIdx.x; g < a.groups; g += gridDim.x, ++it) {
         const uint32_t s = it % kStages;
@@ -131,7 +135,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
                                  a.s_token, a.layer_off, b, pos);
                 if (kbase < 0) flag(a.err_flags, KVW_ERR_PAGE);
                 for (uint32_t r = 0; r < a.R; ++r) bytes += (a.span_hi[r] - a.span_lo[r]) * 8u;
-                if (kbase >= 0) bytes += a.Hk * row_bytes;
+                if (kbase >= 0) bytes += a.Hk * krow_bytes;
             }
         }
         if (early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
@@ -169,19 +173,20 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
         const uint32_t fstarts = __ballot_sync(0xffffffffu, lane < ntok && qok && !fcont);
         if (lane < ntok && qok) {
             if (kbase >= 0 && !kcont) {
-                unsigned char* kdst = st + a.k_off + (size_t)lane * a.Hk * row_bytes;
+                unsigned char* kdst = st + a.k_off + (size_t)lane * a.Hk * krow_bytes;
+                const unsigned char* ksrc = a.cache + kbase * a.kesz;
                 if (a.rows_contig) {
                     uint32_t n = 1;  // run length: up to the next run start
                     while (lane + n < ntok && ((kstarts >> (lane + n)) & 1u) == 0u &&
                            ((qok_mask >> (lane + n)) & 1u) && meta[lane + n].kbase >= 0)
                         ++n;
-                    bulk_load(kdst, a.cache + kbase, n * a.Hk * row_bytes, &full[s]);
+                    bulk_load(kdst, ksrc, n * a.Hk * krow_bytes, &full[s]);
                 } else if (a.heads_contig) {
-                    bulk_load(kdst, a.cache + kbase, a.Hk * row_bytes, &full[s]);
+                    bulk_load(kdst, ksrc, a.Hk * krow_bytes, &full[s]);
                 } else {
                     for (uint32_t h = 0; h < a.Hk; ++h)
-                        bulk_load(kdst + h * row_bytes, a.cache + kbase + (int64_t)h * a.s_head,
-                                  row_bytes, &full[s]);
+                        bulk_load(kdst + h * krow_bytes, ksrc + (int64_t)h * a.s_head * a.kesz,
+                                  krow_bytes, &full[s]);
                 }
             }
             if (a.mode == 0) {
@@ -211,7 +216,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
     }
 }
 
-template <bool INTERLEAVED>
+template <bool INTERLEAVED, bool FP8K>
 __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint64_t* empty,
                                          const unsigned char* stages) {
     const uint32_t tid = threadIdx.x, lane = tid & 31u;
@@ -271,13 +276,18 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
             for (uint32_t h = h_begin; h < h_end; ++h) {
                 const bool is_q = h < a.Hq;
                 if (!is_q && tm.kbase < 0) break;
-                const uint16_t* src =
-                    is_q ? reinterpret_cast<const uint16_t*>(st + a.q_off) + ((size_t)u * a.Hq + h) * a.S
-                         : reinterpret_cast<const uint16_t*>(st + a.k_off) +
-                               ((size_t)u * a.Hk + (h - a.Hq)) * a.S;
                 float va[8], vb[8], ya[8], yb[8];
-                unpack8(*reinterpret_cast<const uint4*>(src + e0), va);
-                unpack8(*reinterpret_cast<const uint4*>(src + e1), vb);
+                if (is_q) {
+                    const uint16_t* src =
+                        reinterpret_cast<const uint16_t*>(st + a.q_off) + ((size_t)u * a.Hq + h) * a.S;
+                    unpack8(*reinterpret_cast<const uint4*>(src + e0), va);
+                    unpack8(*reinterpret_cast<const uint4*>(src + e1), vb);
+                } else {
+                    const unsigned char* src =
+                        st + a.k_off + ((size_t)u * a.Hk + (h - a.Hq)) * a.S * a.kesz;
+                    load_k8<FP8K>(src + e0 * a.kesz, va, a.kscale);
+                    load_k8<FP8K>(src + e1 * a.kesz, vb, a.kscale);
+                }
                 if (INTERLEAVED) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -294,9 +304,10 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
                     st_stream(reinterpret_cast<uint4*>(dst + e0), pack8_bf16(ya));
                     st_stream(reinterpret_cast<uint4*>(dst + e1), pack8_bf16(yb));
                 } else {
-                    uint16_t* dst = a.cache + tm.kbase + (int64_t)(h - a.Hq) * a.s_head;
-                    *reinterpret_cast<uint4*>(dst + e0) = pack8_bf16(ya);
-                    *reinterpret_cast<uint4*>(dst + e1) = pack8_bf16(yb);
+                    unsigned char* dst =
+                        a.cache + (tm.kbase + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
+                    store_k8<FP8K>(dst + e0 * a.kesz, ya, a.kscale);
+                    store_k8<FP8K>(dst + e1 * a.kesz, yb, a.kscale);
                 }
             }
         }
@@ -305,7 +316,7 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
     }
 }
 
-template <bool INTERLEAVED>
+template <bool INTERLEAVED, bool FP8K>
 __global__ void __launch_bounds__(kThreads, 1) qk_rope_kernel(const GqaArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -328,12 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) qk_rope_kernel(const GqaArgs a) {
     if (threadIdx.x >= (unsigned)kConsumers)
         producer(a, full, empty, s_off, s_clen, stages);
     else
-        consumer<INTERLEAVED>(a, full, empty, stages);
+        consumer<INTERLEAVED, FP8K>(a, full, empty, stages);
 }
 
-template <bool INTERLEAVED>
+template <bool INTERLEAVED, bool FP8K>
 cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
-    auto k = qk_rope_kernel<INTERLEAVED>;
+    auto k = qk_rope_kernel<INTERLEAVED, FP8K>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -356,7 +367,7 @@ cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
 // query loads first, then the ragged lookup, then every thread helps gather
 // the tokens' composed (cos, sin) rows into shared memory (one round trip),
 // then key rows are loaded and everything is rotated and stored.
-template <bool INTERLEAVED, int TPB>
+template <bool INTERLEAVED, int TPB, bool FP8K>
 __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
@@ -440,9 +451,16 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
         for (int u = 0; u < TPB; ++u) {
             const int64_t kb = s_kbase[u];
             if (kb >= 0 && !s_bad[u]) {
-                const uint16_t* row = a.cache + kb + (int64_t)(h - a.Hq) * a.s_head;
-                xa[u] = *reinterpret_cast<const uint4*>(row + e0);
-                xb[u] = *reinterpret_cast<const uint4*>(row + e1);
+                const unsigned char* row = a.cache + (kb + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
+                if (FP8K) {  // 8 codes per vector: kept in .x/.y
+                    const uint2 va8 = *reinterpret_cast<const uint2*>(row + e0);
+                    const uint2 vb8 = *reinterpret_cast<const uint2*>(row + e1);
+                    xa[u] = make_uint4(va8.x, va8.y, 0, 0);
+                    xb[u] = make_uint4(vb8.x, vb8.y, 0, 0);
+                } else {
+                    xa[u] = *reinterpret_cast<const uint4*>(row + 2 * e0);
+                    xb[u] = *reinterpret_cast<const uint4*>(row + 2 * e1);
+                }
             }
         }
     }
@@ -465,8 +483,20 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
         const float c[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
         const float s[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
         float va[8], vb[8], ya[8], yb[8];
-        unpack8(xa[u], va);
-        unpack8(xb[u], vb);
+        if (FP8K && !is_q) {
+            unpack8_e4m3(make_uint2(xa[u].x, xa[u].y), va);
+            unpack8_e4m3(make_uint2(xb[u].x, xb[u].y), vb);
+            if (a.kscale != 1.0f) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    va[q] = __fmul_rn(va[q], a.kscale);
+                    vb[q] = __fmul_rn(vb[q], a.kscale);
+                }
+            }
+        } else {
+            unpack8(xa[u], va);
+            unpack8(xb[u], vb);
+        }
         if (INTERLEAVED) {  // pairs (va0,va1) (va2,va3) .. (vb6,vb7)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -477,21 +507,21 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) rope_pair(va[q], vb[q], c[q], s[q], ya[q], yb[q]);
         }
-        uint16_t* row = is_q ? a.q_out + ((uint64_t)t * a.Hq + h) * a.S
-                             : a.cache + s_kbase[u] + (int64_t)(h - a.Hq) * a.s_head;
         if (is_q) {
+            uint16_t* row = a.q_out + ((uint64_t)t * a.Hq + h) * a.S;
             st_stream(reinterpret_cast<uint4*>(row + e0), pack8_bf16(ya));
             st_stream(reinterpret_cast<uint4*>(row + e1), pack8_bf16(yb));
         } else {
-            *reinterpret_cast<uint4*>(row + e0) = pack8_bf16(ya);
-            *reinterpret_cast<uint4*>(row + e1) = pack8_bf16(yb);
+            unsigned char* row = a.cache + (s_kbase[u] + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
+            store_k8<FP8K>(row + e0 * a.kesz, ya, a.kscale);
+            store_k8<FP8K>(row + e1 * a.kesz, yb, a.kscale);
         }
     }
 }
 
-template <bool INTERLEAVED, int TPB>
+template <bool INTERLEAVED, int TPB, bool FP8K>
 cudaError_t launch_staged(const GqaArgs& a, uint32_t threads, size_t smem, cudaStream_t stream) {
-    auto k = qk_rope_staged_kernel<INTERLEAVED, TPB>;
+    auto k = qk_rope_staged_kernel<INTERLEAVED, TPB, FP8K>;
     if (smem > 16 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -515,7 +545,11 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
                                         void* output, uint32_t* err_flags, cudaStream_t stream) {
     using namespace kvw;
     if (!cache) return KVW_EINVAL;
-    if (cache->dtype != KVW_DTYPE_BF16) return KVW_EUNSUPPORTED;
+    if (cache->dtype != KVW_DTYPE_BF16 && cache->dtype != KVW_DTYPE_FP8_E4M3)
+        return KVW_EUNSUPPORTED;
+    const bool fp8 = cache->dtype == KVW_DTYPE_FP8_E4M3;
+    const int64_t esz = fp8 ? 1 : 2;
+    if (fp8 && !(cache->scale > 0.0f && cache->scale < 3.0e38f)) return KVW_EINVAL;
     const uint32_t S = cache->head_size;
     if (S == 0 || S % 16 != 0 || S > kMaxHead) return KVW_EUNSUPPORTED;
     if (num_batches > KVW_MAX_BATCHES) return KVW_EUNSUPPORTED;
@@ -540,8 +574,8 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     if (!aligned16(freqs_cis) || !aligned16(cache->data) ||
         (num_q_heads > 0 && (!aligned16(q_proj) || !aligned16(output))))
         return KVW_EINVAL;
-    if ((cache->stride_page * 2) % 16 || (cache->stride_layer * 2) % 16 ||
-        (cache->stride_token * 2) % 16 || (cache->stride_head * 2) % 16 ||
+    if ((cache->stride_page * esz) % 16 || (cache->stride_layer * esz) % 16 ||
+        (cache->stride_token * esz) % 16 || (cache->stride_head * esz) % 16 ||
         cache->stride_page <= 0 || cache->stride_token <= 0)
         return KVW_EINVAL;
     if (items == 0) return KVW_OK;
@@ -549,7 +583,9 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     GqaArgs a;
     a.q_in = static_cast<const uint16_t*>(q_proj);
     a.q_out = static_cast<uint16_t*>(output);
-    a.cache = static_cast<uint16_t*>(cache->data);
+    a.cache = static_cast<unsigned char*>(cache->data);
+    a.kscale = cache->scale;
+    a.kesz = (uint32_t)esz;
     a.offsets = input_row_offsets;
     a.cache_lengths = cache->cache_lengths;
     a.page_table = cache->page_table;
@@ -594,14 +630,16 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
         int tpb = 4;
         while (tpb > 1 && (uint64_t)(tot_seq_len + tpb - 1) / tpb < 152ull * 4) tpb >>= 1;
         cudaError_t es;
-        if (interleaved)
-            es = tpb == 4 ? launch_staged<true, 4>(a, threads, smem_st, stream)
-               : tpb == 2 ? launch_staged<true, 2>(a, threads, smem_st, stream)
-                          : launch_staged<true, 1>(a, threads, smem_st, stream);
-        else
-            es = tpb == 4 ? launch_staged<false, 4>(a, threads, smem_st, stream)
-               : tpb == 2 ? launch_staged<false, 2>(a, threads, smem_st, stream)
-                          : launch_staged<false, 1>(a, threads, smem_st, stream);
+        auto pick = [&](auto il, auto f8) {
+            constexpr bool IL = decltype(il)::value, F8 = decltype(f8)::value;
+            return tpb == 4 ? launch_staged<IL, 4, F8>(a, threads, smem_st, stream)
+                 : tpb == 2 ? launch_staged<IL, 2, F8>(a, threads, smem_st, stream)
+                            : launch_staged<IL, 1, F8>(a, threads, smem_st, stream);
+        };
+        using T_ = std::true_type;
+        using F_ = std::false_type;
+        es = interleaved ? (fp8 ? pick(T_{}, T_{}) : pick(T_{}, F_{}))
+                         : (fp8 ? pick(F_{}, T_{}) : pick(F_{}, F_{}));
         return es == cudaSuccess ? KVW_OK : KVW_ECUDA;
     }
     a.heads_contig = cache->stride_head == (int64_t)S ? 1u : 0u;
@@ -609,7 +647,8 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
 
     // shared memory: barriers | ragged tables | kStages x (q | k | freqs | meta)
     const uint32_t tables = (uint32_t)(((2ull * num_batches + 1) * 4 + 127) / 128 * 128);
-    const uint64_t per_tok = (uint64_t)(num_q_heads + a.Hk) * S * 2 + (uint64_t)a.R * S * 4 +
+    const uint64_t per_tok = (uint64_t)num_q_heads * S * 2 + (uint64_t)a.Hk * S * esz +
+                             (uint64_t)a.R * S * 4 +
                              sizeof(TokMeta);
     int dev = 0, optin = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -629,7 +668,7 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     auto up16 = [](uint64_t x) { return (uint32_t)((x + 15) / 16 * 16); };
     a.q_off = 0;
     a.k_off = up16(tpb * num_q_heads * S * 2);
-    a.f_off = a.k_off + up16(tpb * a.Hk * S * 2);
+    a.f_off = a.k_off + up16(tpb * a.Hk * S * esz);
     a.meta_off = a.f_off + up16(tpb * a.R * S * 4);
     a.stage_bytes = (uint32_t)((a.meta_off + tpb * sizeof(TokMeta) + 127) / 128 * 128);
     const uint32_t G = S / 16;
@@ -638,6 +677,9 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     if (a.slices > num_q_heads + a.Hk) a.slices = num_q_heads + a.Hk;
     const size_t smem = 128 + (size_t)tables + (size_t)kStages * a.stage_bytes;
     if (smem > (size_t)optin) return KVW_EUNSUPPORTED;
-    const cudaError_t e = interleaved ? launch<true>(a, smem, stream) : launch<false>(a, smem, stream);
+    const cudaError_t e = interleaved ? (fp8 ? launch<true, true>(a, smem, stream)
+                                             : launch<true, false>(a, smem, stream))
+                                      : (fp8 ? launch<false, true>(a, smem, stream)
+                                             : launch<false, false>(a, smem, stream));
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }

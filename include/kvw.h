@@ -168,9 +168,14 @@ int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, const void* 
  *     rotary pairs, s0 + s1 + s2 = head_size / 2).
  * The K row is always the one of the slot position.
  *
+ * An FP8 E4M3 K cache (the collection's scale_dtype_ /
+ * quantization_granularity_ parameters; here a per-tensor scale) is
+ * dequantised (code value times scale, fp32), rotated, and stored again as
+ * satfinite_round_nearest_even(y / scale).
+ *
  *   q_proj         device, bf16 [tot_seq_len, num_q_heads, head_size]
- *   cache          host pointer to the descriptor: bf16, head_size a
- *                  multiple of 16 and <= 512
+ *   cache          host pointer to the descriptor: bf16 or FP8 E4M3 (scale
+ *                  > 0), head_size a multiple of 16 and <= 512
  *   freqs_cis      device, f32 [freqs_rows, head_size]
  *   position_ids   device, uint32 [tot_seq_len] or [3, tot_seq_len], or NULL
  *   mrope_section  HOST, uint32 [3], or NULL

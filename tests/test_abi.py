@@ -106,7 +106,10 @@ def _gqa(cache, T=8, Hq=32, pos=FAKE, sec=None, out=FAKE, layer=1):
     ({}, {"T": 0}, kvw.KVW_OK),
     ({"head_size": 72}, {}, kvw.KVW_EUNSUPPORTED),
     ({"head_size": 1024}, {}, kvw.KVW_EUNSUPPORTED),
-    ({"dtype": kvw.DTYPE_FP8_E4M3}, {}, kvw.KVW_EUNSUPPORTED),
+    ({"dtype": kvw.DTYPE_F32}, {}, kvw.KVW_EUNSUPPORTED),
+    ({"dtype": kvw.DTYPE_FP8_E4M3, "scale": 0.0}, {}, kvw.KVW_EINVAL),
+    ({"dtype": kvw.DTYPE_FP8_E4M3, "strides": (2 * 2 * 16 * 8 * 128, 2 * 16 * 8 * 128,
+                                               16 * 8 * 128, 8 * 128, 136)}, {}, kvw.KVW_EINVAL),
     ({}, {"Hq": 200}, kvw.KVW_EUNSUPPORTED),
     ({}, {"sec": (16, 24, 23)}, kvw.KVW_EINVAL),
     ({}, {"sec": (16, 24, 24), "pos": None}, kvw.KVW_EINVAL),

@@ -183,8 +183,28 @@ def run_gqa(orc, dev, w, alias=False):
     compare_bf16(d.out.host(), out_ref)
     slots = [] if f_ref & 4 else expected_slots(w.offsets, c.cache_lengths, c.page_table,
                                                 c.page_size, c.num_pages)
-    compare_cache(c, d.cache.host(), c_ref, slots, w.layer_idx, fp8=False)
+    compare_cache(c, d.cache.host(), c_ref, slots, w.layer_idx,
+                  fp8=c.dtype == W.DTYPE_FP8_E4M3)
     return d
+
+
+@pytest.mark.parametrize("interleaved", [True, False])
+@pytest.mark.parametrize("mode", [None, "ids", "mrope"])
+def test_gqa_fp8_k_cache_full(orc, dev, interleaved, mode):
+    run_gqa(orc, dev, W.gqa_llama3(interleaved=interleaved, position_mode=mode,
+                                   cache_dtype=W.DTYPE_FP8_E4M3))
+
+
+@pytest.mark.parametrize("scale", [0.5, 3.0])
+@pytest.mark.parametrize("mode", [None, "mrope"])
+def test_gqa_fp8_k_cache_scales_and_layouts(orc, dev, scale, mode):
+    w = W.gqa_workload("f8", 730, [3, 0, 17, 1, 40], [0, 5, 100, 31, 7], 8, 4, 64, page_size=16,
+                       freqs_rows=256, base=10000.0, interleaved=mode is None,
+                       position_mode=mode, mrope_section=(5, 20, 7) if mode else None,
+                       cache_dtype=W.DTYPE_FP8_E4M3, scale=scale)
+    run_gqa(orc, dev, w)
+    w.cache = W.repad_cache(w.cache, 16, 32)  # non-adjacent heads: per-head copies
+    run_gqa(orc, dev, w)
 
 
 @pytest.mark.parametrize("interleaved", [True, False])
