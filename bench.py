@@ -127,6 +127,8 @@ def algorithmic_bytes(w, name):
             return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0) + used
         return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0) + rows * per_row
     c = w.cache
+    if not w.per_head_norm:  # one row of Hk*S values per token
+        return W.algorithmic_bytes_knorm(w.T, 1, w.gamma.size)
     return W.algorithmic_bytes_knorm(w.T, c.num_heads, w.gamma.size)
 
 
@@ -427,7 +429,8 @@ def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=2):
         else:
             kvw.kvw_rms_norm_kv_cache_paged(S["desc"], d.gamma.tensor, w.epsilon,
                                             w.weight_offset, w.layer_idx, w.T, i["off"],
-                                            w.multiply_before_cast, True, o["err"], stream)
+                                            w.multiply_before_cast, w.per_head_norm, o["err"],
+                                            stream)
 
     def step(n, S, comp, first):
         in_ready = torch.cuda.Event()

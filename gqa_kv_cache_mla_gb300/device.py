@@ -143,8 +143,10 @@ class DeviceKNorm(_Base):
         self.err = self._g(np.zeros(1, np.uint32), guard)
         self.desc = _cache_desc(c, self.cache, self.page_table, self.cache_lengths)
 
-    def run(self, stream=None, check=True, per_head_norm=True, **kw):
+    def run(self, stream=None, check=True, per_head_norm=None, **kw):
         w = self.w
+        if per_head_norm is None:
+            per_head_norm = w.per_head_norm
         return kvw.kvw_rms_norm_kv_cache_paged(
             self.desc, self.gamma.tensor, w.epsilon, w.weight_offset, w.layer_idx, w.T,
             self.offsets.tensor, w.multiply_before_cast, per_head_norm, self.err.tensor, stream,

@@ -272,6 +272,28 @@ def mla_workload(name, seed, new_lens, prior_lens, num_heads, page_size, max_seq
     return MLAWorkload(name, q, kv, offsets, freqs, gamma, cache, layer_idx, epsilon)
 
 
+def place_latent_rows(w: MLAWorkload):
+    """Write each new token's 576-wide latent row (w.kv_in) into its cache slot,
+    as the latent projection would before the in-place variant runs: bf16
+    copied, or E4M3 codes of value / scale (library cast) for an FP8 cache."""
+    c = w.cache
+    v = c.view6()
+    P = c.page_size
+    for t, b, pos in new_slots(w.offsets, c.cache_lengths):
+        page = int(c.page_table[b, pos // P])
+        if c.dtype == DTYPE_BF16:
+            v[page, 0, w.layer_idx, pos % P, 0, :] = w.kv_in[t]
+        else:
+            x = (w.kv_in[t].astype(np.uint32) << 16).view(np.float32) / np.float32(c.scale)
+            v[page, 0, w.layer_idx, pos % P, 0, :] = e4m3_bits(x)
+
+
+def context_offsets(cache: PagedCache, offsets) -> np.ndarray:
+    """Ragged offsets over whole contexts (prior + new tokens per request)."""
+    new = np.diff(np.asarray(offsets, dtype=np.int64))
+    return offsets_from_lengths(np.asarray(cache.cache_lengths, dtype=np.int64) + new)
+
+
 def mla_tiny(cache_dtype=DTYPE_BF16, seed=1) -> MLAWorkload:
     """2 requests, new [3,5], prior [0,7], 4 q heads, page 16, max_seq 64, 8 pages."""
     return mla_workload("mla_tiny", seed, [3, 5], [0, 7], num_heads=4, page_size=16,
@@ -371,6 +393,7 @@ class KNormWorkload:
     multiply_before_cast: bool
     cache: PagedCache
     layer_idx: int
+    per_head_norm: bool = True
 
     @property
     def T(self):
@@ -383,7 +406,7 @@ class KNormWorkload:
 
 def knorm_workload(name, seed, new_lens, prior_lens, num_kv_heads, head_size, page_size,
                    gamma_len, weight_offset=0.0, multiply_before_cast=True, num_layers=2,
-                   layer_idx=1, spare_pages=0, epsilon=1e-6) -> KNormWorkload:
+                   layer_idx=1, spare_pages=0, epsilon=1e-6, per_head_norm=True) -> KNormWorkload:
     rng = rng_for(seed)
     new_lens = np.asarray(new_lens, dtype=np.int64)
     prior_lens = np.asarray(prior_lens, dtype=np.int64)
@@ -397,17 +420,20 @@ def knorm_workload(name, seed, new_lens, prior_lens, num_kv_heads, head_size, pa
     fill_new_k_rows(rng, cache, offsets, layer_idx)
     gamma = normal_bf16(rng, (gamma_len,), mean=1.0, std=0.1)
     return KNormWorkload(name, offsets, gamma, epsilon, float(weight_offset),
-                         bool(multiply_before_cast), cache, layer_idx)
+                         bool(multiply_before_cast), cache, layer_idx, bool(per_head_norm))
 
 
-def knorm_paged(gamma_len=128, seed=5, num_requests=64) -> KNormWorkload:
+def knorm_paged(gamma_len=128, seed=5, num_requests=64, weight_offset=0.0,
+                multiply_before_cast=True, per_head_norm=True) -> KNormWorkload:
     """8 kv heads, head 128, page 64; each request decode (p=0.5) or prefill U[64,1024]."""
     rng = rng_for(seed + 1000)
     decode = rng.random(num_requests) < 0.5
     pre = rng.integers(64, 1024, size=num_requests, endpoint=True)
     new = np.where(decode, 1, pre)
     prior = rng.integers(0, 2048, size=num_requests, endpoint=True)
-    return knorm_workload("knorm", seed, new, prior, 8, 128, 64, gamma_len)
+    return knorm_workload("knorm", seed, new, prior, 8, 128, 64, gamma_len,
+                          weight_offset=weight_offset, multiply_before_cast=multiply_before_cast,
+                          per_head_norm=per_head_norm)
 
 
 def algorithmic_bytes_mla(T, H, cache_dtype, distinct_positions=None):
@@ -455,6 +481,14 @@ REGISTRY = {
                  "GQA Llama-3-8B Q/K RoPE, interleaved, FP8 E4M3 K cache (scale 1.0)"),
     "knorm128": (lambda s: knorm_paged(128, seed=s + 3), "rms_norm_kv_cache_paged.cu",
                  "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, G=128"),
+    "knorm128_cast_first": (lambda s: knorm_paged(128, seed=s + 3, weight_offset=0.5,
+                                                  multiply_before_cast=False),
+                            "rms_norm_kv_cache_paged.cu",
+                            "paged K-cache RMSNorm, G=128, multiply_before_cast=false, "
+                            "weight_offset=0.5"),
+    "knorm_whole_row": (lambda s: knorm_paged(1024, seed=s + 3, per_head_norm=False),
+                        "rms_norm_kv_cache_paged.cu",
+                        "paged K-cache RMSNorm over the whole 8x128 K row (per_head_norm=false)"),
     "knorm64": (lambda s: knorm_paged(64, seed=s + 3), "rms_norm_kv_cache_paged.cu",
                 "paged K-cache RMSNorm: 8 kv heads x 128, page 64, 64 mixed requests, "
                 "subset G=64"),

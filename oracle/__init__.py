@@ -58,8 +58,19 @@ def _load(path):
                               ctypes.c_float, ctypes.c_int)
     L.oracle_mla_rope_rmsnorm_quant.restype = u32
     L.oracle_mla_rope_rmsnorm_quant.argtypes = [
-        vp, vp, vp, u32, u32, u32, vp, u32, vp, vp, i64, vp, i32, f32, vp, u32, vp,
+        vp, i32, vp, vp, u32, u32, u32, vp, u32, vp, vp, i64, vp, i32, f32, vp, u32, vp,
         u32, u32, u32, u32, u32, i64, i64, i64, i64, i64, u32, f32, i32]
+    L.oracle_mla_rope_rmsnorm_inplace.restype = u32
+    L.oracle_mla_rope_rmsnorm_inplace.argtypes = [
+        vp, i32, vp, vp, u32, u32, u32, vp, u32, vp, vp, i32, f32, vp, u32, vp, u32, u32, u32,
+        i64, i64, i64, u32, f32, i32]
+    L.oracle_convert_bf16_to_e4m3.restype = None
+    L.oracle_convert_bf16_to_e4m3.argtypes = [vp, vp, i64, f32]
+    L.oracle_quantize_rows_e4m3.restype = None
+    L.oracle_quantize_rows_e4m3.argtypes = [vp, i64, vp, i64, vp, i64, i64]
+    L.oracle_mla_gather_latent.restype = u32
+    L.oracle_mla_gather_latent.argtypes = [
+        vp, i32, f32, vp, i32, f32, vp, u32, u32, u32, u32, i64, i64, i64, u32, vp, u32, u32]
     L.oracle_qk_rope_paged_ragged.restype = u32
     L.oracle_qk_rope_paged_ragged.argtypes = [
         vp, vp, u32, u32, u32, vp, i32, f32, vp, u32, vp, u32, u32, u32, u32, u32, i64, i64,
@@ -104,7 +115,9 @@ class Variant:
         g = globals()
         for name in ("bf16_encode", "bf16_decode", "e4m3_encode", "e4m3_decode",
                      "rope_pairs_f32", "rms_inv", "rms_norm_f32", "mla_rope_rmsnorm_quant",
-                     "qk_rope_paged_ragged", "rms_norm_kv_cache_paged", "has_openmp"):
+                     "qk_rope_paged_ragged", "rms_norm_kv_cache_paged", "has_openmp",
+                     "mla_rope_rmsnorm_inplace", "convert_bf16_to_e4m3", "quantize_rows_e4m3",
+                     "mla_gather_latent", "_q_out_buffer"):
             fn = g[name]
             setattr(self, name, types.FunctionType(fn.__code__, dict(g, lib=lambda: self._L),
                                                    name, fn.__defaults__, fn.__closure__))
@@ -176,19 +189,24 @@ def _c(a, dt):
     return np.ascontiguousarray(a, dtype=dt)
 
 
+def _q_out_buffer(q, q_rope_out, out_dtype):
+    if q_rope_out is None:
+        q_rope_out = np.zeros(q.shape, dtype=np.uint16 if out_dtype == 0 else np.uint8)
+    return q_rope_out
+
+
 def mla_rope_rmsnorm_quant(w, q_rope_out=None, cache_data=None, nthreads=1, T=None,
-                           kv_row_stride=None, kv_in=None):
+                           kv_row_stride=None, kv_in=None, out_dtype=0):
     """Run the MLA write on workload ``w``.
 
     Returns ``(q_rope_out, cache_data, flags)``.  ``cache_data`` defaults to a
-    copy of ``w.cache.data`` and ``q_rope_out`` to zeros; both are modified in
-    place when given.
+    copy of ``w.cache.data`` and ``q_rope_out`` to zeros (bf16 bits, or E4M3
+    codes with ``out_dtype`` 1); both are modified in place when given.
     """
     c = w.cache
     T = w.T if T is None else T
     q = _c(w.q_rope, np.uint16)
-    if q_rope_out is None:
-        q_rope_out = np.zeros(q.shape, dtype=np.uint16)
+    q_rope_out = _q_out_buffer(q, q_rope_out, out_dtype)
     if cache_data is None:
         cache_data = c.data.copy()
     kv = _c(w.kv_in if kv_in is None else kv_in, np.uint16)
@@ -198,12 +216,63 @@ def mla_rope_rmsnorm_quant(w, q_rope_out=None, cache_data=None, nthreads=1, T=No
     g = _c(w.gamma, np.uint16)
     s = c.strides
     flags = lib().oracle_mla_rope_rmsnorm_quant(
-        _p(q_rope_out), _p(q), _p(off), len(off) - 1, T, q.shape[1] if q.ndim == 3 else 0,
-        _p(fr), fr.shape[0], _p(g), _p(kv), stride, _p(cache_data), c.dtype, c.scale,
-        _p(c.page_table), c.max_pages_per_seq, _p(c.cache_lengths), c.num_pages,
-        c.num_layers, c.page_size, c.num_heads, c.head_size, s[0], s[1], s[2], s[3], s[4],
-        w.layer_idx, w.epsilon, nthreads)
+        _p(q_rope_out), out_dtype, _p(q), _p(off), len(off) - 1, T,
+        q.shape[1] if q.ndim == 3 else 0, _p(fr), fr.shape[0], _p(g), _p(kv), stride,
+        _p(cache_data), c.dtype, c.scale, _p(c.page_table), c.max_pages_per_seq,
+        _p(c.cache_lengths), c.num_pages, c.num_layers, c.page_size, c.num_heads, c.head_size,
+        s[0], s[1], s[2], s[3], s[4], w.layer_idx, w.epsilon, nthreads)
     return q_rope_out, cache_data, int(flags)
+
+
+def mla_rope_rmsnorm_inplace(w, q_rope_out=None, cache_data=None, nthreads=1, out_dtype=0):
+    """In-place variant: the new latent rows are read from ``w.cache`` (place
+    them with ``workloads.place_latent_rows``).  Returns (q_out, cache, flags)."""
+    c = w.cache
+    q = _c(w.q_rope, np.uint16)
+    q_rope_out = _q_out_buffer(q, q_rope_out, out_dtype)
+    if cache_data is None:
+        cache_data = c.data.copy()
+    off = _c(w.offsets, np.uint32)
+    fr = _c(w.freqs, np.float32)
+    g = _c(w.gamma, np.uint16)
+    s = c.strides
+    flags = lib().oracle_mla_rope_rmsnorm_inplace(
+        _p(q_rope_out), out_dtype, _p(q), _p(off), len(off) - 1, w.T,
+        q.shape[1] if q.ndim == 3 else 0, _p(fr), fr.shape[0], _p(g), _p(cache_data), c.dtype,
+        c.scale, _p(c.page_table), c.max_pages_per_seq, _p(c.cache_lengths), c.num_pages,
+        c.num_layers, c.page_size, s[0], s[2], s[3], w.layer_idx, w.epsilon, nthreads)
+    return q_rope_out, cache_data, int(flags)
+
+
+def convert_bf16_to_e4m3(x_bits, scale=1.0) -> np.ndarray:
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_convert_bf16_to_e4m3(_p(x), _p(out), x.size, scale)
+    return out
+
+
+def quantize_rows_e4m3(x_bits):
+    """Per-row dynamic FP8: returns (codes uint8 [rows, cols], scales f32 [rows])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    out = np.empty(x.shape, dtype=np.uint8)
+    sc = np.empty(rows, dtype=np.float32)
+    lib().oracle_quantize_rows_e4m3(_p(x), cols, _p(out), cols, _p(sc), rows, cols)
+    return out, sc
+
+
+def mla_gather_latent(cache, layer_idx, ctx_offsets, out_dtype=0, out_scale=1.0, out=None):
+    """Paged -> contiguous latent rows; returns (out [rows, 576], flags)."""
+    off = np.ascontiguousarray(ctx_offsets, dtype=np.uint32)
+    rows = int(off[-1]) if off.size else 0
+    if out is None:
+        out = np.zeros((rows, 576), dtype=np.uint16 if out_dtype == 0 else np.uint8)
+    s = cache.strides
+    flags = lib().oracle_mla_gather_latent(
+        _p(out), out_dtype, out_scale, _p(cache.data), cache.dtype, cache.scale,
+        _p(cache.page_table), cache.max_pages_per_seq, cache.num_pages, cache.num_layers,
+        cache.page_size, s[0], s[2], s[3], layer_idx, _p(off), len(off) - 1, rows)
+    return out, int(flags)
 
 
 def qk_rope_paged_ragged(w, output=None, cache_data=None, nthreads=1, T=None):
@@ -229,8 +298,10 @@ def qk_rope_paged_ragged(w, output=None, cache_data=None, nthreads=1, T=None):
     return output, cache_data, int(flags)
 
 
-def rms_norm_kv_cache_paged(w, cache_data=None, nthreads=1, per_head_norm=True, T=None):
+def rms_norm_kv_cache_paged(w, cache_data=None, nthreads=1, per_head_norm=None, T=None):
     """Run the in-place K-cache RMSNorm on workload ``w``; returns (cache, flags)."""
+    if per_head_norm is None:
+        per_head_norm = getattr(w, "per_head_norm", True)
     c = w.cache
     T = w.T if T is None else T
     if cache_data is None:

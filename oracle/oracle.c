@@ -266,7 +266,7 @@ static int64_t slot_base(const orc_layout* L, uint32_t b, uint64_t pos, uint32_t
  *      cache row of slot pos in layer layer_idx (head 0).
  */
 uint32_t oracle_mla_rope_rmsnorm_quant(
-    uint16_t* q_rope_out, const uint16_t* q_rope, const uint32_t* offsets, uint32_t B,
+    void* q_rope_out, int out_dtype, const uint16_t* q_rope, const uint32_t* offsets, uint32_t B,
     uint32_t T, uint32_t H, const float* freqs, uint32_t freqs_rows, const uint16_t* gamma,
     const uint16_t* kv_in, int64_t kv_row_stride, void* cache, int cache_dtype, float scale,
     const uint32_t* page_table, uint32_t max_pages, const uint32_t* cache_lengths,
@@ -303,13 +303,14 @@ uint32_t oracle_mla_rope_rmsnorm_quant(
         /* 1a. q rope, every head */
         for (uint32_t h = 0; h < H; ++h) {
             const uint16_t* xq = q_rope + ((int64_t)t * H + h) * ROPE;
-            uint16_t* yq = q_rope_out + ((int64_t)t * H + h) * ROPE;
+            const int64_t yo = ((int64_t)t * H + h) * ROPE;
             for (uint32_t k = 0; k < ROPE / 2; ++k) {
                 float y0, y1;
                 rope_pair(oracle_bf16_to_f32(xq[2 * k]), oracle_bf16_to_f32(xq[2 * k + 1]),
                           cs[2 * k], cs[2 * k + 1], &y0, &y1);
-                yq[2 * k] = oracle_f32_to_bf16(y0);
-                yq[2 * k + 1] = oracle_f32_to_bf16(y1);
+                /* bf16, or E4M3 by direct saturating conversion (no scale) */
+                store_elem(q_rope_out, yo + 2 * k, out_dtype, 1.0f, y0);
+                store_elem(q_rope_out, yo + 2 * k + 1, out_dtype, 1.0f, y1);
             }
         }
         /* the cache row this token writes */
@@ -332,6 +333,140 @@ uint32_t oracle_mla_rope_rmsnorm_quant(
     }
     free(tok_b);
     free(tok_i);
+    return flags;
+}
+
+/* Value of cache element idx: bf16 widened, or E4M3 decoded times scale. */
+static float load_elem(const void* base, int64_t idx, int dtype, float scale) {
+    if (dtype == ORC_BF16) return oracle_bf16_to_f32(((const uint16_t*)base)[idx]);
+    return oracle_e4m3_to_f32(((const uint8_t*)base)[idx]) * scale;
+}
+
+/*
+ * fused_rope_rmsnorm_kernel ("mla_graph" module page; first two steps of the
+ * MLA decode and prefill branches): the same computation as above, but the
+ * 576-wide latent rows of the new tokens are already in the cache (written by
+ * the latent projection) and are normalised and rotated in place; the cache
+ * may be bf16 or FP8 E4M3 (dequantised with its scale, re-quantised after).
+ */
+uint32_t oracle_mla_rope_rmsnorm_inplace(
+    void* q_rope_out, int out_dtype, const uint16_t* q_rope, const uint32_t* offsets, uint32_t B,
+    uint32_t T, uint32_t H, const float* freqs, uint32_t freqs_rows, const uint16_t* gamma,
+    void* cache, int cache_dtype, float scale, const uint32_t* page_table, uint32_t max_pages,
+    const uint32_t* cache_lengths, uint32_t num_pages, uint32_t num_layers, uint32_t page_size,
+    int64_t s_page, int64_t s_layer, int64_t s_token, uint32_t layer_idx, float eps, int nthreads) {
+    const uint32_t NORM = 512, ROPE = 64, ROW = 576;
+    if (T == 0) return 0;
+    if (!offsets_valid(offsets, B, T)) return ORC_FLAG_OFFSETS;
+    orc_layout L = {num_pages, num_layers, page_size, 1, ROW, max_pages,
+                    s_page, 0, s_layer, s_token, ROW, page_table};
+    uint32_t* tok_b = (uint32_t*)malloc(sizeof(uint32_t) * T);
+    uint32_t* tok_i = (uint32_t*)malloc(sizeof(uint32_t) * T);
+    token_map(offsets, B, tok_b, tok_i);
+    float g[512];
+    for (uint32_t j = 0; j < NORM; ++j) g[j] = oracle_bf16_to_f32(gamma[j]);
+    uint32_t flags = 0;
+    int64_t t;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) reduction(| : flags) schedule(static)
+    for (t = 0; t < (int64_t)T; ++t) {
+        uint32_t b = tok_b[t];
+        uint64_t pos = (uint64_t)cache_lengths[b] + tok_i[t];
+        if (pos >= freqs_rows) {
+            flags |= ORC_FLAG_POS;
+            continue;
+        }
+        const float* cs = freqs + pos * ROPE;
+        for (uint32_t h = 0; h < H; ++h) {
+            const uint16_t* xq = q_rope + ((int64_t)t * H + h) * ROPE;
+            const int64_t yo = ((int64_t)t * H + h) * ROPE;
+            for (uint32_t k = 0; k < ROPE / 2; ++k) {
+                float y0, y1;
+                rope_pair(oracle_bf16_to_f32(xq[2 * k]), oracle_bf16_to_f32(xq[2 * k + 1]),
+                          cs[2 * k], cs[2 * k + 1], &y0, &y1);
+                store_elem(q_rope_out, yo + 2 * k, out_dtype, 1.0f, y0);
+                store_elem(q_rope_out, yo + 2 * k + 1, out_dtype, 1.0f, y1);
+            }
+        }
+        uint32_t f = 0;
+        int64_t base = slot_base(&L, b, pos, layer_idx, &f);
+        flags |= f;
+        if (base < 0) continue;
+        float row[576], y[576];
+        for (uint32_t j = 0; j < ROW; ++j) row[j] = load_elem(cache, base + j, cache_dtype, scale);
+        for (uint32_t k = 0; k < ROPE / 2; ++k)
+            rope_pair(row[NORM + 2 * k], row[NORM + 2 * k + 1], cs[2 * k], cs[2 * k + 1],
+                      &y[NORM + 2 * k], &y[NORM + 2 * k + 1]);
+        oracle_rms_norm_f32(row, g, NORM, eps, y);
+        for (uint32_t j = 0; j < ROW; ++j) store_elem(cache, base + j, cache_dtype, scale, y[j]);
+    }
+    free(tok_b);
+    free(tok_i);
+    return flags;
+}
+
+/*
+ * convert_bf16_to_fp8_e4m3fn ("mla_graph" module page): n bf16 values to
+ * E4M3 codes, satfinite_rne(x / scale).
+ */
+void oracle_convert_bf16_to_e4m3(const uint16_t* in, uint8_t* out, int64_t n, float scale) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_e4m3(oracle_bf16_to_f32(in[i]) / scale);
+}
+
+/*
+ * Dynamic FP8 scaling ("mla_graph" module page), per row (token): the scale
+ * of a row is amax(|x|) / 448 (1 for an all-zero row) and its codes are
+ * satfinite_rne(x / scale), so the row's largest magnitude maps to 448.
+ */
+void oracle_quantize_rows_e4m3(const uint16_t* in, int64_t in_stride, uint8_t* out,
+                               int64_t out_stride, float* scales, int64_t rows, int64_t cols) {
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int64_t c = 0; c < cols; ++c) {
+            float a = fabsf(oracle_bf16_to_f32(in[r * in_stride + c]));
+            if (a > amax) amax = a;
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scales[r] = sc;
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * out_stride + c] = oracle_f32_to_e4m3(oracle_bf16_to_f32(in[r * in_stride + c]) / sc);
+    }
+}
+
+/*
+ * Paged -> contiguous copy of the MLA latent cache (the step after the
+ * in-place RoPE/RMSNorm in the FP8 prefill branch): request b's context rows
+ * (positions 0 .. ctx_offsets[b+1] - ctx_offsets[b] - 1 of its cache) are
+ * copied to out rows ctx_offsets[b] .. ctx_offsets[b+1]-1, converted from
+ * the cache type (bf16, or E4M3 times cache_scale) to the output type (bf16
+ * round to nearest even, or E4M3 satfinite_rne(v / out_scale)).  Flags:
+ * 4 when ctx_offsets do not start at 0, decrease or do not end at rows;
+ * 1 for a row without a valid page (the row is not written).
+ */
+uint32_t oracle_mla_gather_latent(void* out, int out_dtype, float out_scale, const void* cache,
+                                  int cache_dtype, float cache_scale, const uint32_t* page_table,
+                                  uint32_t max_pages, uint32_t num_pages, uint32_t num_layers,
+                                  uint32_t page_size, int64_t s_page, int64_t s_layer,
+                                  int64_t s_token, uint32_t layer_idx, const uint32_t* ctx_offsets,
+                                  uint32_t B, uint32_t rows) {
+    const uint32_t ROW = 576;
+    if (rows == 0) return 0;
+    if (!offsets_valid(ctx_offsets, B, rows)) return ORC_FLAG_OFFSETS;
+    orc_layout L = {num_pages, num_layers, page_size, 1, ROW, max_pages,
+                    s_page, 0, s_layer, s_token, ROW, page_table};
+    uint32_t flags = 0;
+    for (uint32_t b = 0; b < B; ++b) {
+        for (uint32_t r = ctx_offsets[b]; r < ctx_offsets[b + 1]; ++r) {
+            uint64_t pos = r - ctx_offsets[b];
+            uint32_t f = 0;
+            int64_t base = slot_base(&L, b, pos, layer_idx, &f);
+            flags |= f;
+            if (base < 0) continue;
+            for (uint32_t j = 0; j < ROW; ++j)
+                store_elem(out, (int64_t)r * ROW + j, out_dtype, out_scale,
+                           load_elem(cache, base + j, cache_dtype, cache_scale));
+        }
+    }
     return flags;
 }
 

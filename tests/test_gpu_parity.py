@@ -378,3 +378,9 @@ def test_max_batches_all_entry_points(orc, dev):
     run_gqa(orc, dev, g)
     k = W.knorm_workload("mb", 904, new, prior, 2, 64, page_size=32, gamma_len=64)
     run_knorm(orc, dev, k)
+
+
+@pytest.mark.parametrize("name", ["knorm128_cast_first", "knorm_whole_row"])
+def test_knorm_variant_configs_full(orc, dev, name):
+    w = W.REGISTRY[name][0](2)
+    run_knorm(orc, dev, w, per_head_norm=w.per_head_norm)
