@@ -44,11 +44,13 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 
 WORKLOADS = W.REGISTRY
-DEFAULT_SEED = {"mla": 2, "gqa": 2, "kno": 2}
+DEFAULT_SEED = 2
 
 
-def kind(name):
-    return name[:3]
+def kind_of(w):
+    """mla | gqa | kno | gather | codec, from the workload's type."""
+    return {W.MLAWorkload: "mla", W.GQAWorkload: "gqa", W.KNormWorkload: "kno",
+            W.GatherWorkload: "gather", W.ConvertWorkload: "codec"}[type(w)]
 
 
 def combine_ranks(ms, tokens, world, device=None):
@@ -101,35 +103,42 @@ def ncu_traffic(workload, kernel_file):
     return float(m.group(1))
 
 
-def algorithmic_bytes(w, name):
-    k = kind(name)
+def algorithmic_bytes(w, name=None):
+    """Bytes one launch must move: every distinct byte read or written once."""
+    k = kind_of(w)
     if k == "mla":
         c = w.cache
         pos = np.concatenate([c.cache_lengths[b] + np.arange(w.offsets[b + 1] - w.offsets[b])
                               for b in range(w.B)]) if w.T else np.zeros(0)
-        return W.algorithmic_bytes_mla(w.T, w.H, c.dtype, len(np.unique(pos)))
+        q_out = 2 if w.q_out_dtype == W.DTYPE_BF16 else 1
+        row_in = c.elem_bytes if w.inplace else 2  # in place: the row comes from the cache
+        return (w.T * (w.H * W.MLA_ROPE_DIM * (2 + q_out) + W.MLA_ROW * (row_in + c.elem_bytes))
+                + len(np.unique(pos)) * W.MLA_ROPE_DIM * 4)
     if k == "gqa":
         c = w.cache
+        kb = c.elem_bytes
         if w.position_ids is None:
             rows = len(np.unique(np.concatenate(
                 [c.cache_lengths[b] + np.arange(w.offsets[b + 1] - w.offsets[b])
                  for b in range(w.B)])))
             return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, rows,
-                                           c.elem_bytes)
-        # mrope / ids: each distinct (row, pair-range) read counts; bound by distinct rows
-        rows = len(np.unique(w.position_ids))
-        per_row = c.head_size * 4
-        if w.mrope_section is not None:
-            # every position row supplies only its section's pairs
-            used = 0
-            for r, sec in enumerate(w.mrope_section):
-                used += len(np.unique(w.position_ids[r])) * int(sec) * 8
-            return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0) + used
-        return W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0) + rows * per_row
-    c = w.cache
-    if not w.per_head_norm:  # one row of Hk*S values per token
-        return W.algorithmic_bytes_knorm(w.T, 1, w.gamma.size)
-    return W.algorithmic_bytes_knorm(w.T, c.num_heads, w.gamma.size)
+                                           kb)
+        base = W.algorithmic_bytes_gqa(w.T, w.q_proj.shape[1], c.num_heads, c.head_size, 0, kb)
+        if w.mrope_section is not None:  # each position row supplies only its section's pairs
+            return base + sum(len(np.unique(w.position_ids[r])) * int(sec) * 8
+                              for r, sec in enumerate(w.mrope_section))
+        return base + len(np.unique(w.position_ids)) * c.head_size * 4
+    if k == "kno":
+        c = w.cache
+        if not w.per_head_norm:  # one row of Hk*S values per token
+            return W.algorithmic_bytes_knorm(w.T, 1, w.gamma.size)
+        return W.algorithmic_bytes_knorm(w.T, c.num_heads, w.gamma.size)
+    if k == "gather":
+        out_b = 2 if w.out_dtype == W.DTYPE_BF16 else 1
+        return w.rows * W.MLA_ROW * (w.cache.elem_bytes + out_b)
+    if w.per_row:
+        return w.x.size * 3 + w.x.shape[0] * 4
+    return w.x.size * 3
 
 
 class ClockSampler:
@@ -194,18 +203,32 @@ def cpu_baseline(w, name, budget_s):
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     if not oracle.has_openmp():
         threads = 1
-    k = kind(name)
-    cache = w.cache.data.copy()  # written in place by every call (allocated once)
+    k = kind_of(w)
     if k == "mla":
-        q_out = np.zeros_like(w.q_rope)
-        fn = lambda: oracle.mla_rope_rmsnorm_quant(w, q_rope_out=q_out, cache_data=cache,
-                                                   nthreads=threads)
+        cache = w.cache.data.copy()  # written in place by every call (allocated once)
+        q_out = np.zeros(w.q_rope.shape, np.uint16 if w.q_out_dtype == 0 else np.uint8)
+        if w.inplace:
+            fn = lambda: oracle.mla_rope_rmsnorm_inplace(w, q_rope_out=q_out, cache_data=cache,
+                                                         nthreads=threads, out_dtype=w.q_out_dtype)
+        else:
+            fn = lambda: oracle.mla_rope_rmsnorm_quant(w, q_rope_out=q_out, cache_data=cache,
+                                                       nthreads=threads, out_dtype=w.q_out_dtype)
     elif k == "gqa":
+        cache = w.cache.data.copy()
         out = np.zeros_like(w.q_proj)
         fn = lambda: oracle.qk_rope_paged_ragged(w, output=out, cache_data=cache,
                                                  nthreads=threads)
-    else:
+    elif k == "kno":
+        cache = w.cache.data.copy()
         fn = lambda: oracle.rms_norm_kv_cache_paged(w, cache_data=cache, nthreads=threads)
+    elif k == "gather":
+        threads = 1
+        fn = lambda: oracle.mla_gather_latent(w.cache, w.layer_idx, w.ctx_offsets, w.out_dtype,
+                                              w.out_scale)
+    else:
+        threads = 1
+        fn = ((lambda: oracle.quantize_rows_e4m3(w.x)) if w.per_row
+              else (lambda: oracle.convert_bf16_to_e4m3(w.x, w.scale)))
     fn()  # warm: page in buffers
     n, t0 = 0, time.perf_counter()
     while True:
@@ -215,8 +238,9 @@ def cpu_baseline(w, name, budget_s):
         if el >= budget_s:
             break
     tps = n * w.T / el
-    return {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": "%d whole batches of %d tokens (%s), %.1f s wall" % (n, w.T, name, el),
+    return {"value": tps, "unit": "tokens/s" if k not in ("gather", "codec") else "rows/s",
+            "cores": threads, "kind": "oracle",
+            "sample": "%d whole batches of %d units (%s), %.1f s wall" % (n, w.T, name, el),
             "gbs": algorithmic_bytes(w, name) * n / el / 1e9}
 
 
@@ -225,7 +249,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     name = args.workload
-    w = WORKLOADS[name][0](DEFAULT_SEED[kind(name)])
+    w = WORKLOADS[name][0](DEFAULT_SEED)
     import oracle
 
     oracle.build()
@@ -240,16 +264,20 @@ def run_reference(args):
             times.append(w.T / cb["value"])
     ms = 1000.0 * statistics.mean(times)
     value = w.T / (ms / 1000.0)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+    unit = "tokens/s" if kind_of(w) in ("mla", "gqa", "kno") else "rows/s"
+    line = {"impl": "reference",
+            "metric": METRIC if name == "mla_decode" else "%s %s; achieved HBM GB/s vs peak" % (
+                name, unit),
+            "value": value, "unit": unit,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": name + ": " + WORKLOADS[name][2], "tokens": w.T},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads,
                              "kind": "oracle",
                              "sample": "each step: whole %d-token batches for %.2f s" %
                                        (w.T, step_s)},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -270,9 +298,10 @@ def run_ours(args):
     name = args.workload
     builder, kfile, desc = WORKLOADS[name]
     # replicas: each rank writes its own independent batch (weak scaling)
-    w = builder(DEFAULT_SEED[kind(name)] + 100 * rank)
-    k = kind(name)
-    cls = {"mla": D.DeviceMLA, "gqa": D.DeviceGQA, "kno": D.DeviceKNorm}[k]
+    w = builder(DEFAULT_SEED + 100 * rank)
+    k = kind_of(w)
+    cls = {"mla": D.DeviceMLA, "gqa": D.DeviceGQA, "kno": D.DeviceKNorm,
+           "gather": D.DeviceGather, "codec": D.DeviceConvert}[k]
     d = cls(w, device=dev, guard=False)
     stream = torch.cuda.current_stream(dev)
     run = lambda: d.run(stream=stream)
@@ -317,12 +346,15 @@ def run_ours(args):
     ms = statistics.mean(per)
     ms_max, tokens_all = combine_ranks(ms, w.T, world, dev)
     value = tokens_all / (ms_max / 1000.0)
+    unit = "tokens/s" if k in ("mla", "gqa", "kno") else "rows/s"
     assert d.flags() == 0, "kernel reported data errors on the benchmark inputs"
+    if k == "mla" and w.inplace:  # restore the rows the in-place steps rewrote
+        d.cache.reset(w.cache.data)
 
     # end to end through the public API: pinned host inputs -> device, launch,
     # q/output and the error word back to the host, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and k in ("mla", "gqa", "kno") and not getattr(w, "inplace", False):
         e2e = measure_e2e(d, w, k, stream, dev, max(3, min(args.steps, 200)), args.warmup)
         e2e["ms"], _ = combine_ranks(e2e["ms"], w.T, world, dev)
         e2e = {"value": tokens_all / (e2e["ms"] / 1000.0), "unit": "tokens/s",
@@ -347,16 +379,18 @@ def run_ours(args):
     if rank != 0:
         return 0
     line = {
-        "metric": METRIC if k == "mla" else "%s tokens/s; achieved HBM GB/s vs peak" % name,
-        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": (METRIC if name == "mla_decode" else
+                   "%s %s; achieved HBM GB/s vs peak" % (name, unit)),
+        "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes and distributions of the benchmark configs)",
         "config": {"workload": name + ": " + desc, "tokens_per_gpu": w.T,
                    "l2": ("flushed before every step (512 MiB written, 512 MiB read)" if flush
                           else "inputs larger than L2 (%.2f GB per step)" % (abytes / 1e9)),
-                   "io": "bf16 activations in, fp32 arithmetic, cache out %s" %
-                         ("e4m3" if getattr(w.cache, "dtype", 0) == W.DTYPE_FP8_E4M3 else "bf16"),
+                   "io": "bf16 in, fp32 arithmetic, %s out" %
+                         ("e4m3" if (getattr(getattr(w, "cache", None), "dtype", 0) ==
+                                     W.DTYPE_FP8_E4M3 or k == "codec") else "bf16"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
         "clocks": clk,

@@ -11,4 +11,4 @@ extern "C" const char* kvw_status_string(int status) {
     }
 }
 
-extern "C" int kvw_version(void) { return 100; }
+extern "C" int kvw_version(void) { return 110; }

@@ -89,13 +89,18 @@ __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&
 
 // One warp per token: RMSNorm of the latent part, RoPE of the rope part,
 // quantise, write the 576-wide cache row.
-template <bool FP8>
+// INPLACE: the latent row is not read from kv_in but from the cache slot
+// it is written back to (bf16, or E4M3 dequantised with the cache scale).
+template <bool FP8, bool INPLACE>
 __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
     const bool active = t < a.T;
     uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
-    if (active) {
+    if (INPLACE && active) {
+        g0 = ld_table(a.gamma + lane);
+        g1 = ld_table(a.gamma + 32 + lane);
+    } else if (active) {
         const uint4* row = reinterpret_cast<const uint4*>(a.kv_in + (int64_t)t * a.kv_row_stride);
         x0 = ld_stream(row + lane);
         x1 = ld_stream(row + 32 + lane);
@@ -127,9 +132,18 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         fb = ld_table(fr + 1);
     }
     // RMSNorm of the 512 latent values held 16 per lane.
-    float v0[8], v1[8], w0[8], w1[8];
-    unpack8(x0, v0);
-    unpack8(x1, v1);
+    float v0[8], v1[8], w0[8], w1[8], xv[8];
+    if (INPLACE) {
+        constexpr int64_t esz = FP8 ? 1 : 2;
+        const unsigned char* rowb = static_cast<const unsigned char*>(a.cache) + base * esz;
+        load_k8<FP8>(rowb + (int64_t)lane * 8 * esz, v0, a.scale);
+        load_k8<FP8>(rowb + (int64_t)(256 + lane * 8) * esz, v1, a.scale);
+        if (lane < 8) load_k8<FP8>(rowb + (int64_t)(kNorm + lane * 8) * esz, xv, a.scale);
+    } else {
+        unpack8(x0, v0);
+        unpack8(x1, v1);
+        unpack8(xr, xv);
+    }
     unpack8(g0, w0);
     unpack8(g1, w1);
     float ss = 0.0f;
@@ -149,8 +163,7 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
     store8<FP8>(a.cache, base + lane * 8, y0, a.scale);
     store8<FP8>(a.cache, base + 256 + lane * 8, y1, a.scale);
     if (lane < 8) {  // rope part: 4 adjacent pairs per lane
-        float xv[8], yr[8];
-        unpack8(xr, xv);
+        float yr[8];
         rope_pair(xv[0], xv[1], fa.x, fa.y, yr[0], yr[1]);
         rope_pair(xv[2], xv[3], fa.z, fa.w, yr[2], yr[3]);
         rope_pair(xv[4], xv[5], fb.x, fb.y, yr[4], yr[5]);
@@ -160,7 +173,8 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
 }
 
 // q_rope streaming: VPT 16-byte vectors per thread.
-template <int VPT>
+// QF8: q_rope_output is E4M3 (direct saturating conversion) instead of bf16.
+template <int VPT, bool QF8>
 __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
     __shared__ uint32_t s_pos[(kThreads * VPT) / 8 + 2];
     const uint32_t qb = blockIdx.x - a.kv_blocks;
@@ -217,24 +231,27 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
         rope_pair(xv[2], xv[3], fa.z, fa.w, y[2], y[3]);
         rope_pair(xv[4], xv[5], fb.x, fb.y, y[4], y[5]);
         rope_pair(xv[6], xv[7], fb.z, fb.w, y[6], y[7]);
-        st_stream(a.q_out + v, pack8_bf16(y));
+        if (QF8)
+            reinterpret_cast<uint2*>(a.q_out)[v] = pack8_e4m3(y);
+        else
+            st_stream(a.q_out + v, pack8_bf16(y));
     }
 }
 
-template <bool FP8, int VPT>
+template <bool FP8, int VPT, bool QF8, bool INPLACE>
 __global__ void __launch_bounds__(kThreads) mla_rope_rmsnorm_quant_kernel(const MlaArgs a) {
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
     uint32_t* s_clen = s_dyn + a.B + 1;
     if (blockIdx.x < a.kv_blocks)
-        latent_rows<FP8>(a, s_off, s_clen);
+        latent_rows<FP8, INPLACE>(a, s_off, s_clen);
     else
-        q_rows<VPT>(a, s_off, s_clen);
+        q_rows<VPT, QF8>(a, s_off, s_clen);
 }
 
-template <bool FP8, int VPT>
+template <bool FP8, int VPT, bool QF8, bool INPLACE>
 cudaError_t launch(const MlaArgs& a, uint32_t blocks, size_t smem, cudaStream_t stream) {
-    auto k = mla_rope_rmsnorm_quant_kernel<FP8, VPT>;
+    auto k = mla_rope_rmsnorm_quant_kernel<FP8, VPT, QF8, INPLACE>;
     if (smem > 32 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -244,15 +261,51 @@ cudaError_t launch(const MlaArgs& a, uint32_t blocks, size_t smem, cudaStream_t 
 }
 
 // CTAs of this kernel that fit on the device at once (all SMs).
-template <bool FP8, int VPT>
+template <bool FP8, int VPT, bool QF8, bool INPLACE>
 uint64_t resident_ctas(size_t smem) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, mla_rope_rmsnorm_quant_kernel<FP8, VPT>, kThreads, smem) != cudaSuccess)
+            &per_sm, mla_rope_rmsnorm_quant_kernel<FP8, VPT, QF8, INPLACE>, kThreads, smem) !=
+        cudaSuccess)
         return 0;
     return (uint64_t)sms * (uint64_t)per_sm;
+}
+
+// Grid sizing and launch of one instance.  Vectors per thread: the smallest
+// of 1, 2, 4 whose grid fits in one wave of resident CTAs (a decode step is
+// latency-bound: a second wave would double its duration); 4 when nothing
+// fits (long prefill launches, where many short CTAs keep the memory system
+// busy).
+template <bool FP8, bool QF8, bool INPLACE>
+cudaError_t launch_sized(const MlaArgs& a, uint64_t qvec, size_t smem, cudaStream_t stream) {
+    int vpt = 4;
+    for (int cand : {1, 2}) {
+        const uint64_t qb = (qvec + (uint64_t)kThreads * cand - 1) / ((uint64_t)kThreads * cand);
+        const uint64_t cap = cand == 1 ? resident_ctas<FP8, 1, QF8, INPLACE>(smem)
+                                       : resident_ctas<FP8, 2, QF8, INPLACE>(smem);
+        if (a.kv_blocks + qb <= cap) {
+            vpt = cand;
+            break;
+        }
+    }
+    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
+    const uint64_t blocks = a.kv_blocks + qblocks;
+    if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+    return vpt == 1 ? launch<FP8, 1, QF8, INPLACE>(a, (uint32_t)blocks, smem, stream)
+         : vpt == 2 ? launch<FP8, 2, QF8, INPLACE>(a, (uint32_t)blocks, smem, stream)
+                    : launch<FP8, 4, QF8, INPLACE>(a, (uint32_t)blocks, smem, stream);
+}
+
+template <bool INPLACE>
+cudaError_t dispatch(const MlaArgs& a, bool fp8, bool qf8, uint64_t qvec, size_t smem,
+                     cudaStream_t stream) {
+    if (fp8)
+        return qf8 ? launch_sized<true, true, INPLACE>(a, qvec, smem, stream)
+                   : launch_sized<true, false, INPLACE>(a, qvec, smem, stream);
+    return qf8 ? launch_sized<false, true, INPLACE>(a, qvec, smem, stream)
+               : launch_sized<false, false, INPLACE>(a, qvec, smem, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -260,35 +313,40 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 }  // namespace kvw
 
-extern "C" int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, const void* q_rope,
-                                          const uint32_t* input_row_offsets, uint32_t num_batches,
-                                          uint32_t tot_seq_len, uint32_t num_heads,
-                                          const void* freqs_cis, int32_t freq_dtype,
-                                          uint32_t freqs_rows, const void* gamma,
-                                          int32_t gamma_dtype, const void* kv_in,
-                                          int64_t kv_row_stride, const kvw_paged_cache_t* cache,
-                                          uint32_t layer_idx, float epsilon, uint32_t* err_flags,
-                                          cudaStream_t stream) {
-    using namespace kvw;
+namespace kvw {
+namespace {
+
+// Validation and launch shared by the fused and the in-place entry points.
+int mla_entry(void* q_rope_out, int32_t out_dtype, const void* q_rope,
+              const uint32_t* input_row_offsets, uint32_t num_batches, uint32_t tot_seq_len,
+              uint32_t num_heads, const void* freqs_cis, int32_t freq_dtype, uint32_t freqs_rows,
+              const void* gamma, int32_t gamma_dtype, const void* kv_in, int64_t kv_row_stride,
+              const kvw_paged_cache_t* cache, uint32_t layer_idx, float epsilon,
+              uint32_t* err_flags, cudaStream_t stream, bool inplace) {
     if (!cache) return KVW_EINVAL;
-    if (out_dtype != KVW_DTYPE_BF16 || freq_dtype != KVW_DTYPE_F32 || gamma_dtype != KVW_DTYPE_BF16)
+    if ((out_dtype != KVW_DTYPE_BF16 && out_dtype != KVW_DTYPE_FP8_E4M3) ||
+        freq_dtype != KVW_DTYPE_F32 || gamma_dtype != KVW_DTYPE_BF16)
         return KVW_EUNSUPPORTED;
     if (cache->dtype != KVW_DTYPE_BF16 && cache->dtype != KVW_DTYPE_FP8_E4M3) return KVW_EUNSUPPORTED;
     if (cache->head_size != kRow || cache->num_heads != 1) return KVW_EUNSUPPORTED;
     if (num_batches > KVW_MAX_BATCHES) return KVW_EUNSUPPORTED;
     if (tot_seq_len == 0) return KVW_OK;
     const bool fp8 = cache->dtype == KVW_DTYPE_FP8_E4M3;
+    const bool qf8 = out_dtype == KVW_DTYPE_FP8_E4M3;
     const int64_t esz = fp8 ? 1 : 2;
-    if (!input_row_offsets || !freqs_cis || !gamma || !kv_in || !cache->data || !cache->page_table ||
+    if (!input_row_offsets || !freqs_cis || !gamma || !cache->data || !cache->page_table ||
         !cache->cache_lengths)
         return KVW_EINVAL;
+    if (!inplace && !kv_in) return KVW_EINVAL;
     if (num_heads > 0 && (!q_rope || !q_rope_out)) return KVW_EINVAL;
     if (layer_idx >= cache->num_layers || cache->page_size == 0 || freqs_rows == 0 ||
         cache->max_pages_per_seq == 0)
         return KVW_EINVAL;
-    if (!(fp8 ? cache->scale > 0.0f : true) || !(epsilon >= 0.0f)) return KVW_EINVAL;
-    if (kv_row_stride < (int64_t)kRow || kv_row_stride % 8 != 0) return KVW_EINVAL;
-    if (!aligned16(freqs_cis) || !aligned16(gamma) || !aligned16(kv_in) || !aligned16(cache->data) ||
+    if (!(fp8 ? (cache->scale > 0.0f && cache->scale < 3.0e38f) : true) || !(epsilon >= 0.0f))
+        return KVW_EINVAL;
+    if (!inplace && (kv_row_stride < (int64_t)kRow || kv_row_stride % 8 != 0)) return KVW_EINVAL;
+    if (!aligned16(freqs_cis) || !aligned16(gamma) || (!inplace && !aligned16(kv_in)) ||
+        !aligned16(cache->data) ||
         (num_heads > 0 && (!aligned16(q_rope) || !aligned16(q_rope_out))))
         return KVW_EINVAL;
     if ((cache->stride_page * esz) % 16 || (cache->stride_layer * esz) % 16 ||
@@ -323,34 +381,41 @@ extern "C" int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, c
     a.kv_blocks = (tot_seq_len + kRowsPerKvBlock - 1) / kRowsPerKvBlock;
     a.eps = epsilon;
     a.scale = cache->scale;
-
-    // Vectors per thread: the smallest of 1, 2, 4 whose grid fits in one wave
-    // of resident CTAs (a decode step is latency-bound: a second wave would
-    // double its duration); 4 when nothing fits (long prefill launches, where
-    // many short CTAs keep the memory system busy).
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
-    int vpt = 4;
-    for (int cand : {1, 2}) {
-        const uint64_t qb = (qvec + (uint64_t)kThreads * cand - 1) / ((uint64_t)kThreads * cand);
-        const uint64_t cap = fp8 ? (cand == 1 ? resident_ctas<true, 1>(smem) : resident_ctas<true, 2>(smem))
-                                 : (cand == 1 ? resident_ctas<false, 1>(smem) : resident_ctas<false, 2>(smem));
-        if (a.kv_blocks + qb <= cap) {
-            vpt = cand;
-            break;
-        }
-    }
-    const uint64_t qblocks = (qvec + (uint64_t)kThreads * vpt - 1) / ((uint64_t)kThreads * vpt);
-    const uint64_t blocks = a.kv_blocks + qblocks;
-    if (blocks > 0x7fffffffull) return KVW_EUNSUPPORTED;
-    cudaError_t e;
-    if (fp8) {
-        e = vpt == 4 ? launch<true, 4>(a, (uint32_t)blocks, smem, stream)
-          : vpt == 2 ? launch<true, 2>(a, (uint32_t)blocks, smem, stream)
-                     : launch<true, 1>(a, (uint32_t)blocks, smem, stream);
-    } else {
-        e = vpt == 4 ? launch<false, 4>(a, (uint32_t)blocks, smem, stream)
-          : vpt == 2 ? launch<false, 2>(a, (uint32_t)blocks, smem, stream)
-                     : launch<false, 1>(a, (uint32_t)blocks, smem, stream);
-    }
+    const cudaError_t e = inplace ? dispatch<true>(a, fp8, qf8, qvec, smem, stream)
+                                  : dispatch<false>(a, fp8, qf8, qvec, smem, stream);
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
+}
+
+}  // namespace
+}  // namespace kvw
+
+extern "C" int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, const void* q_rope,
+                                          const uint32_t* input_row_offsets, uint32_t num_batches,
+                                          uint32_t tot_seq_len, uint32_t num_heads,
+                                          const void* freqs_cis, int32_t freq_dtype,
+                                          uint32_t freqs_rows, const void* gamma,
+                                          int32_t gamma_dtype, const void* kv_in,
+                                          int64_t kv_row_stride, const kvw_paged_cache_t* cache,
+                                          uint32_t layer_idx, float epsilon, uint32_t* err_flags,
+                                          cudaStream_t stream) {
+    return kvw::mla_entry(q_rope_out, out_dtype, q_rope, input_row_offsets, num_batches,
+                          tot_seq_len, num_heads, freqs_cis, freq_dtype, freqs_rows, gamma,
+                          gamma_dtype, kv_in, kv_row_stride, cache, layer_idx, epsilon, err_flags,
+                          stream, false);
+}
+
+extern "C" int kvw_mla_rope_rmsnorm_inplace(void* q_rope_out, int32_t out_dtype,
+                                            const void* q_rope, const uint32_t* input_row_offsets,
+                                            uint32_t num_batches, uint32_t tot_seq_len,
+                                            uint32_t num_heads, const void* freqs_cis,
+                                            int32_t freq_dtype, uint32_t freqs_rows,
+                                            const void* gamma, int32_t gamma_dtype,
+                                            const kvw_paged_cache_t* cache, uint32_t layer_idx,
+                                            float epsilon, uint32_t* err_flags,
+                                            cudaStream_t stream) {
+    return kvw::mla_entry(q_rope_out, out_dtype, q_rope, input_row_offsets, num_batches,
+                          tot_seq_len, num_heads, freqs_cis, freq_dtype, freqs_rows, gamma,
+                          gamma_dtype, nullptr, 0, cache, layer_idx, epsilon, err_flags, stream,
+                          true);
 }

@@ -81,7 +81,10 @@ class DeviceMLA(_Base):
         self.w, self.device, self.buffers = w, device, []
         c = w.cache
         self.q = self._g(w.q_rope, guard)
-        self.q_out_init = np.full(w.q_rope.shape, q_out_fill, np.uint16)
+        if w.q_out_dtype == W.DTYPE_BF16:
+            self.q_out_init = np.full(w.q_rope.shape, q_out_fill, np.uint16)
+        else:
+            self.q_out_init = np.full(w.q_rope.shape, q_out_fill & 0xFF, np.uint8)
         self.q_out = self._g(self.q_out_init, guard)
         self.kv = self._g(w.kv_in, guard)
         self.offsets = self._g(w.offsets, guard)
@@ -97,6 +100,12 @@ class DeviceMLA(_Base):
         w = self.w
         kw.setdefault("num_heads", w.q_rope.shape[1])
         kw.setdefault("tot_seq_len", w.T)
+        kw.setdefault("out_dtype", w.q_out_dtype)
+        if w.inplace:
+            return kvw.kvw_mla_rope_rmsnorm_inplace(
+                self.q_out.tensor, self.q.tensor, self.offsets.tensor, self.freqs.tensor,
+                self.gamma.tensor, self.desc, w.layer_idx, w.epsilon, self.err.tensor, stream,
+                check=check, **kw)
         kw.setdefault("kv_row_stride", w.kv_in.shape[-1])
         return kvw.kvw_mla_rope_rmsnorm_quant(
             self.q_out.tensor, self.q.tensor, self.offsets.tensor, self.freqs.tensor,
@@ -151,3 +160,48 @@ class DeviceKNorm(_Base):
             self.desc, self.gamma.tensor, w.epsilon, w.weight_offset, w.layer_idx, w.T,
             self.offsets.tensor, w.multiply_before_cast, per_head_norm, self.err.tensor, stream,
             check=check, **kw)
+
+
+class DeviceGather(_Base):
+    def __init__(self, w: W.GatherWorkload, device="cuda", guard=True):
+        self.w, self.device, self.buffers = w, device, []
+        c = w.cache
+        self.cache = self._g(c.data, guard)
+        self.page_table = self._g(c.page_table, guard)
+        self.cache_lengths = self._g(c.cache_lengths, guard)
+        self.ctx = self._g(w.ctx_offsets, guard)
+        self.out_init = np.zeros((w.rows, 576), np.uint16 if w.out_dtype == W.DTYPE_BF16
+                                 else np.uint8)
+        self.out = self._g(self.out_init, guard)
+        self.err = self._g(np.zeros(1, np.uint32), guard)
+        self.desc = _cache_desc(c, self.cache, self.page_table, self.cache_lengths)
+
+    def run(self, stream=None, check=True):
+        w = self.w
+        return kvw.kvw_mla_gather_latent(self.out.tensor, w.out_dtype, w.out_scale, self.desc,
+                                         w.layer_idx, self.ctx.tensor, self.err.tensor, stream,
+                                         total_rows=w.rows, check=check)
+
+
+class DeviceConvert(_Base):
+    def __init__(self, w: W.ConvertWorkload, device="cuda", guard=True):
+        self.w, self.device, self.buffers = w, device, []
+        self.x = self._g(w.x, guard)
+        self.out = self._g(np.zeros(w.x.shape, np.uint8), guard)
+        self.scales = self._g(np.zeros(w.x.shape[0] if w.per_row else 1, np.float32), guard)
+        self.err = self._g(np.zeros(1, np.uint32), guard)  # unused: no data errors here
+
+    def run(self, stream=None, check=True):
+        w = self.w
+        if w.per_row:
+            return kvw.kvw_quantize_fp8_rows(self.out.tensor, self.scales.tensor, self.x.tensor,
+                                             stream, check=check)
+        return kvw.kvw_convert_bf16_to_fp8_e4m3(self.out.tensor, self.x.tensor, w.scale, stream,
+                                                check=check)
+
+
+def for_workload(w, device="cuda", guard=True):
+    """The Device* holder matching the type of workload ``w``."""
+    cls = {W.MLAWorkload: DeviceMLA, W.GQAWorkload: DeviceGQA, W.KNormWorkload: DeviceKNorm,
+           W.GatherWorkload: DeviceGather, W.ConvertWorkload: DeviceConvert}[type(w)]
+    return cls(w, device=device, guard=guard)

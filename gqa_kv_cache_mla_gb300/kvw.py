@@ -70,6 +70,15 @@ def _load():
     L.kvw_rms_norm_kv_cache_paged.restype = ctypes.c_int
     L.kvw_rms_norm_kv_cache_paged.argtypes = [pc, vp, u32, f32, f32, u32, u32, vp, u32,
                                               ctypes.c_int, ctypes.c_int, vp, vp]
+    L.kvw_mla_rope_rmsnorm_inplace.restype = ctypes.c_int
+    L.kvw_mla_rope_rmsnorm_inplace.argtypes = [vp, i32, vp, vp, u32, u32, u32, vp, i32, u32, vp,
+                                               i32, pc, u32, f32, vp, vp]
+    L.kvw_mla_gather_latent.restype = ctypes.c_int
+    L.kvw_mla_gather_latent.argtypes = [vp, i32, f32, pc, u32, vp, u32, u32, vp, vp]
+    L.kvw_convert_bf16_to_fp8_e4m3.restype = ctypes.c_int
+    L.kvw_convert_bf16_to_fp8_e4m3.argtypes = [vp, vp, ctypes.c_uint64, f32, vp]
+    L.kvw_quantize_fp8_rows.restype = ctypes.c_int
+    L.kvw_quantize_fp8_rows.argtypes = [vp, vp, vp, u32, u32, i64, i64, vp]
     L.kvw_status_string.restype = ctypes.c_char_p
     L.kvw_status_string.argtypes = [ctypes.c_int]
     L.kvw_version.restype = ctypes.c_int
@@ -153,6 +162,52 @@ def kvw_mla_rope_rmsnorm_quant(q_rope_out, q_rope, input_row_offsets, freqs_cis,
         _ptr(freqs_cis), freq_dtype, rows, _ptr(gamma), gamma_dtype, _ptr(kv_in), stride,
         ctypes.byref(cache), layer_idx, epsilon, _ptr(err_flags), _stream(stream))
     return _done(st, "kvw_mla_rope_rmsnorm_quant", check)
+
+
+def kvw_mla_rope_rmsnorm_inplace(q_rope_out, q_rope, input_row_offsets, freqs_cis, gamma,
+                                 cache: PagedCacheT, layer_idx: int, epsilon: float,
+                                 err_flags=None, stream=None, *, num_batches=None,
+                                 tot_seq_len=None, num_heads=None, freqs_rows=None,
+                                 out_dtype=DTYPE_BF16, freq_dtype=DTYPE_F32,
+                                 gamma_dtype=DTYPE_BF16, check=True) -> int:
+    B = input_row_offsets.shape[0] - 1 if num_batches is None else num_batches
+    T = q_rope.shape[0] if tot_seq_len is None else tot_seq_len
+    H = q_rope.shape[1] if num_heads is None else num_heads
+    rows = freqs_cis.shape[0] if freqs_rows is None else freqs_rows
+    st = lib.kvw_mla_rope_rmsnorm_inplace(
+        _ptr(q_rope_out), out_dtype, _ptr(q_rope), _ptr(input_row_offsets), B, T, H,
+        _ptr(freqs_cis), freq_dtype, rows, _ptr(gamma), gamma_dtype, ctypes.byref(cache),
+        layer_idx, epsilon, _ptr(err_flags), _stream(stream))
+    return _done(st, "kvw_mla_rope_rmsnorm_inplace", check)
+
+
+def kvw_mla_gather_latent(out, out_dtype: int, out_scale: float, cache: PagedCacheT,
+                          layer_idx: int, ctx_offsets, err_flags=None, stream=None, *,
+                          num_batches=None, total_rows=None, check=True) -> int:
+    B = ctx_offsets.shape[0] - 1 if num_batches is None else num_batches
+    rows = out.shape[0] if total_rows is None else total_rows
+    st = lib.kvw_mla_gather_latent(_ptr(out), out_dtype, out_scale, ctypes.byref(cache),
+                                   layer_idx, _ptr(ctx_offsets), B, rows, _ptr(err_flags),
+                                   _stream(stream))
+    return _done(st, "kvw_mla_gather_latent", check)
+
+
+def kvw_convert_bf16_to_fp8_e4m3(out, inp, scale: float = 1.0, stream=None, *, n=None,
+                                 check=True) -> int:
+    n = inp.numel() if n is None else n
+    st = lib.kvw_convert_bf16_to_fp8_e4m3(_ptr(out), _ptr(inp), n, scale, _stream(stream))
+    return _done(st, "kvw_convert_bf16_to_fp8_e4m3", check)
+
+
+def kvw_quantize_fp8_rows(out_codes, out_scales, inp, stream=None, *, rows=None, cols=None,
+                          in_row_stride=None, out_row_stride=None, check=True) -> int:
+    rows = inp.shape[0] if rows is None else rows
+    cols = inp.shape[1] if cols is None else cols
+    ins = inp.stride(0) if in_row_stride is None else in_row_stride
+    outs = out_codes.stride(0) if out_row_stride is None else out_row_stride
+    st = lib.kvw_quantize_fp8_rows(_ptr(out_codes), _ptr(out_scales), _ptr(inp), rows, cols, ins,
+                                   outs, _stream(stream))
+    return _done(st, "kvw_quantize_fp8_rows", check)
 
 
 def kvw_qk_rope_paged_ragged(q_proj, input_row_offsets, cache: PagedCacheT, freqs_cis,

@@ -25,13 +25,12 @@ def main():
     a = ap.parse_args()
     builder, _, desc = W.REGISTRY[a.workload]
     w = builder(a.seed)
-    cls = {"mla": D.DeviceMLA, "gqa": D.DeviceGQA, "kno": D.DeviceKNorm}[a.workload[:3]]
-    d = cls(w, device="cuda", guard=False)
+    d = D.for_workload(w, device="cuda", guard=False)
     for _ in range(a.warmup + a.launches):
         d.run()
     torch.cuda.synchronize()
     assert d.flags() == 0
-    print("%s: %d launches (%s), tokens=%d" % (a.workload, a.warmup + a.launches, desc, w.T))
+    print("%s: %d launches (%s), units=%d" % (a.workload, a.warmup + a.launches, desc, w.T))
     return 0
 
 

@@ -238,6 +238,8 @@ class MLAWorkload:
     cache: PagedCache
     layer_idx: int
     epsilon: float
+    inplace: bool = False  # latent rows already in the cache (in-place variant)
+    q_out_dtype: int = DTYPE_BF16
 
     @property
     def T(self):
@@ -292,6 +294,76 @@ def context_offsets(cache: PagedCache, offsets) -> np.ndarray:
     """Ragged offsets over whole contexts (prior + new tokens per request)."""
     new = np.diff(np.asarray(offsets, dtype=np.int64))
     return offsets_from_lengths(np.asarray(cache.cache_lengths, dtype=np.int64) + new)
+
+
+def mla_inplace(w: MLAWorkload) -> MLAWorkload:
+    """The same step for the in-place variant: latent rows placed in the cache."""
+    place_latent_rows(w)
+    w.inplace = True
+    return w
+
+
+def fill_contexts(rng, cache: PagedCache, offsets, layer_idx):
+    """N(0,1) latent rows (bf16, or E4M3 codes of value / scale) in every
+    context slot (prior and new tokens) of every request."""
+    ctx = context_offsets(cache, offsets)
+    v = cache.view6()
+    P = cache.page_size
+    for b in range(len(ctx) - 1):
+        n = int(ctx[b + 1]) - int(ctx[b])
+        if n == 0:
+            continue
+        x = rng.standard_normal(size=(n, cache.head_size), dtype=np.float32)
+        rows = bf16_bits(x) if cache.dtype == DTYPE_BF16 else e4m3_bits(x / np.float32(cache.scale))
+        for p in range(n):
+            v[int(cache.page_table[b, p // P]), 0, layer_idx, p % P, 0, :] = rows[p]
+    return ctx
+
+
+@dataclasses.dataclass
+class GatherWorkload:
+    name: str
+    cache: PagedCache
+    layer_idx: int
+    ctx_offsets: np.ndarray  # uint32 [B+1] over whole contexts
+    out_dtype: int
+    out_scale: float
+
+    @property
+    def rows(self):
+        return int(self.ctx_offsets[-1])
+
+    @property
+    def T(self):
+        return self.rows
+
+
+def mla_gather(w: MLAWorkload, out_dtype=DTYPE_FP8_E4M3, out_scale=1.0, seed=9) -> GatherWorkload:
+    ctx = fill_contexts(rng_for(seed), w.cache, w.offsets, w.layer_idx)
+    return GatherWorkload(w.name + "_gather", w.cache, w.layer_idx, ctx, out_dtype, out_scale)
+
+
+@dataclasses.dataclass
+class ConvertWorkload:
+    name: str
+    x: np.ndarray  # bf16 bits, flat (convert) or [rows, cols] (per-row quantisation)
+    scale: float = 1.0
+    per_row: bool = False
+
+    @property
+    def T(self):
+        return int(self.x.shape[0]) if self.per_row else int(self.x.size)
+
+
+def fp8_convert(n=1 << 26, seed=10, scale=1.0) -> ConvertWorkload:
+    """bf16 weights N(0, 0.05) (n values) to E4M3."""
+    return ConvertWorkload("fp8_convert", normal_bf16(rng_for(seed), (n,), std=0.05), scale)
+
+
+def fp8_quant_rows(rows=32768, cols=2048, seed=11) -> ConvertWorkload:
+    """Per-token dynamic FP8 of activations: rows of N(0,1) with 1% outliers x20."""
+    x = normal_bf16(rng_for(seed), (rows, cols), outlier_frac=0.01)
+    return ConvertWorkload("fp8_quant_rows", x, 1.0, per_row=True)
 
 
 def mla_tiny(cache_dtype=DTYPE_BF16, seed=1) -> MLAWorkload:
@@ -467,6 +539,24 @@ REGISTRY = {
                         "mla_rope_rmsnorm_quant.cu",
                         "MLA ragged prefill: 16 req, new U[512,8192], H=128, 1% outliers x20, "
                         "FP8 E4M3 cache"),
+    "mla_decode_fp8q": (lambda s: dataclasses.replace(mla_decode(DTYPE_FP8_E4M3, seed=s),
+                                                      q_out_dtype=DTYPE_FP8_E4M3),
+                        "mla_rope_rmsnorm_quant.cu",
+                        "MLA decode DeepSeek-V3, FP8 cache and FP8 q_rope output"),
+    "mla_decode_inplace": (lambda s: mla_inplace(mla_decode(DTYPE_FP8_E4M3, seed=s)),
+                           "mla_rope_rmsnorm_quant.cu",
+                           "MLA decode DeepSeek-V3, in-place variant on an FP8 cache"),
+    "mla_prefill_inplace": (lambda s: mla_inplace(mla_prefill(DTYPE_BF16, seed=s + 1)),
+                            "mla_rope_rmsnorm_quant.cu",
+                            "MLA ragged prefill, in-place variant on a bf16 cache"),
+    "mla_gather_prefill": (lambda s: mla_gather(mla_prefill(DTYPE_BF16, seed=s + 1)),
+                           "mla_gather_latent.cu",
+                           "paged->contiguous latent gather of the prefill contexts, bf16 "
+                           "cache to FP8 E4M3 (scale 1)"),
+    "fp8_convert": (lambda s: fp8_convert(seed=s + 10), "fp8_codec.cu",
+                    "bf16 -> E4M3 conversion of 2^26 values"),
+    "fp8_quant_rows": (lambda s: fp8_quant_rows(seed=s + 11), "fp8_codec.cu",
+                       "per-row dynamic FP8 of a [32768, 2048] bf16 activation"),
     "mla_prefill_bf16_4req": (lambda s: mla_prefill(DTYPE_BF16, seed=s + 1, num_requests=4),
                               "mla_rope_rmsnorm_quant.cu",
                               "MLA ragged prefill, 4 of the 16 requests (profiling size), bf16 cache"),

@@ -131,7 +131,9 @@ typedef struct kvw_paged_cache {
  * freqs_cis[pos][2k+1] (sine).  quant is bf16 round-to-nearest-even, or the
  * FP8 rule of the descriptor's scale.
  *
- *   q_rope_out     device, [tot_seq_len, num_heads, 64], out_dtype (bf16)
+ *   q_rope_out     device, [tot_seq_len, num_heads, 64], out_dtype: bf16, or
+ *                  FP8 E4M3 by direct saturating conversion (no scale; the
+ *                  out_rope_dtype parameter of the page)
  *   q_rope         device, bf16 [tot_seq_len, num_heads, 64], contiguous
  *   input_row_offsets, num_batches   ragged boundaries (see above)
  *   tot_seq_len    host-known number of new tokens (= offsets[num_batches])
@@ -153,6 +155,67 @@ int kvw_mla_rope_rmsnorm_quant(void* q_rope_out, int32_t out_dtype, const void* 
                                int32_t gamma_dtype, const void* kv_in, int64_t kv_row_stride,
                                const kvw_paged_cache_t* cache, uint32_t layer_idx, float epsilon,
                                uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * In-place variant ("mla_graph" module page, entry fused_rope_rmsnorm_kernel;
+ * the first two steps of the MLA decode and prefill branches): identical to
+ * kvw_mla_rope_rmsnorm_quant except that each new token's 576-wide latent
+ * row is read from its cache slot (written there by the latent projection)
+ * and the normalised / rotated row is written back to the same slot.  A bf16
+ * cache is read and written as bf16; an FP8 E4M3 cache is dequantised with
+ * its scale, and re-quantised after.  Arguments as above without kv_in.
+ */
+int kvw_mla_rope_rmsnorm_inplace(void* q_rope_out, int32_t out_dtype, const void* q_rope,
+                                 const uint32_t* input_row_offsets, uint32_t num_batches,
+                                 uint32_t tot_seq_len, uint32_t num_heads, const void* freqs_cis,
+                                 int32_t freq_dtype, uint32_t freqs_rows, const void* gamma,
+                                 int32_t gamma_dtype, const kvw_paged_cache_t* cache,
+                                 uint32_t layer_idx, float epsilon, uint32_t* err_flags,
+                                 cudaStream_t stream);
+
+/*
+ * Paged -> contiguous copy of the MLA latent cache ("mla_graph" module page,
+ * entry mla_prefill_branch_fp8: the KV latent values are copied out of the
+ * paged cache into a contiguous buffer and quantised).  Request b's context
+ * (cache positions 0 .. ctx_offsets[b+1] - ctx_offsets[b] - 1, i.e. prior plus
+ * new tokens) is copied to out rows ctx_offsets[b] .. ctx_offsets[b+1] - 1.
+ * Values are read as the cache holds them (bf16, or E4M3 times the cache
+ * scale) and written as out_dtype: bf16 (round to nearest even) or FP8 E4M3
+ * satfinite_round_nearest_even(v / out_scale).
+ *
+ *   out            device, [total_rows, 576] of out_dtype, 16-byte aligned
+ *   cache          host pointer to the descriptor (num_heads 1, head_size 576)
+ *   ctx_offsets    device, uint32 [num_batches + 1]: 0, non-decreasing, ending
+ *                  at total_rows (else KVW_ERR_OFFSETS and nothing is written)
+ * A row whose slot has no valid page is not written (KVW_ERR_PAGE).
+ */
+int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_scale,
+                          const kvw_paged_cache_t* cache, uint32_t layer_idx,
+                          const uint32_t* ctx_offsets, uint32_t num_batches, uint32_t total_rows,
+                          uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * bf16 -> FP8 E4M3 ("mla_graph" module page, convert_bf16_to_fp8_e4m3fn):
+ * out[i] = satfinite_round_nearest_even(in[i] / scale), n a multiple of 8.
+ *   out  device, n bytes, 8-byte aligned;  in  device, n bf16, 16-byte aligned
+ */
+int kvw_convert_bf16_to_fp8_e4m3(void* out, const void* in, uint64_t n, float scale,
+                                 cudaStream_t stream);
+
+/*
+ * Dynamic FP8 scaling per row ("mla_graph" module page: dynamic FP8 scaling
+ * of the FP8 branches; per-token granularity): for each row r,
+ *   out_scales[r] = max_j |in[r][j]| / 448   (1 for an all-zero row)
+ *   out_codes[r][j] = satfinite_round_nearest_even(in[r][j] / out_scales[r])
+ * so the row's largest magnitude becomes +-448 and in ~= code * scale.
+ *   in          device, bf16 rows of `cols` values, row stride in_row_stride
+ *               elements (multiple of 8, 16-byte aligned); cols a multiple of 8
+ *   out_codes   device, uint8 rows, row stride out_row_stride (multiple of 8)
+ *   out_scales  device, f32 [rows]
+ */
+int kvw_quantize_fp8_rows(void* out_codes, float* out_scales, const void* in, uint32_t rows,
+                          uint32_t cols, int64_t in_row_stride, int64_t out_row_stride,
+                          cudaStream_t stream);
 
 /*
  * Fused GQA Q/K RoPE ("generic_fused_qk_rope_bshd_paged_ragged" page,

@@ -105,3 +105,15 @@ def compare_bf16(gpu, ref):
         u = bf16_ulp_diff(gpu[diff], ref[diff])
         assert u.max() <= 1, "bf16 difference above 1 ulp: %d" % int(u.max())
     return int(diff.size)
+
+
+def compare_e4m3(gpu, ref, max_frac=1e-3):
+    """E4M3 codes equal except 1-ulp flips on at most max_frac of them."""
+    gpu = np.asarray(gpu).reshape(-1)
+    ref = np.asarray(ref).reshape(-1)
+    diff = np.flatnonzero(gpu != ref)
+    if diff.size:
+        u = e4m3_ulp_diff(gpu[diff], ref[diff])
+        assert u.max() <= 1, "fp8 difference above 1 ulp: %d" % int(u.max())
+        assert diff.size <= max(1, max_frac * gpu.size), diff.size / gpu.size
+    return int(diff.size)

@@ -15,8 +15,10 @@ ODD = 0x10008   # an 8-byte but not 16-byte aligned address
 
 def test_exports_every_header_function():
     names = kvw.header_functions()
-    assert set(names) == {"kvw_mla_rope_rmsnorm_quant", "kvw_qk_rope_paged_ragged",
-                          "kvw_rms_norm_kv_cache_paged", "kvw_status_string", "kvw_version"}
+    assert set(names) == {"kvw_mla_rope_rmsnorm_quant", "kvw_mla_rope_rmsnorm_inplace",
+                          "kvw_qk_rope_paged_ragged", "kvw_rms_norm_kv_cache_paged",
+                          "kvw_mla_gather_latent", "kvw_convert_bf16_to_fp8_e4m3",
+                          "kvw_quantize_fp8_rows", "kvw_status_string", "kvw_version"}
     for n in names:
         assert hasattr(kvw.lib, n)
     out = subprocess.run(["nm", "-D", "--defined-only", kvw.LIB_PATH], capture_output=True,
@@ -26,7 +28,7 @@ def test_exports_every_header_function():
 
 
 def test_status_strings_and_version():
-    assert kvw.version() == 100
+    assert kvw.version() == 110
     assert kvw.status_string(0) == "KVW_OK"
     for s in (1, 2, 3):
         assert kvw.status_string(s).startswith("KVW_E")
@@ -60,7 +62,7 @@ def _mla(cache, **kw):
 
 @pytest.mark.parametrize("cache_kw,call_kw,want", [
     ({}, {"T": 0}, kvw.KVW_OK),  # nothing to do: no launch
-    ({}, {"out_dtype": kvw.DTYPE_FP8_E4M3}, kvw.KVW_EUNSUPPORTED),
+    ({}, {"out_dtype": kvw.DTYPE_F32}, kvw.KVW_EUNSUPPORTED),
     ({}, {"freq_dtype": kvw.DTYPE_BF16}, kvw.KVW_EUNSUPPORTED),
     ({"head_size": 512}, {}, kvw.KVW_EUNSUPPORTED),
     ({"num_heads": 2}, {}, kvw.KVW_EUNSUPPORTED),
@@ -142,3 +144,50 @@ def test_binding_raises_on_error_status():
     with pytest.raises(kvw.KvwError):
         kvw._done(kvw.KVW_EINVAL, "x", True)
     assert kvw._done(kvw.KVW_EINVAL, "x", False) == kvw.KVW_EINVAL
+
+
+
+def test_inplace_host_checks():
+    c = _mla_cache()
+    f = kvw.lib.kvw_mla_rope_rmsnorm_inplace
+    args = [FAKE, kvw.DTYPE_BF16, FAKE, FAKE, 2, 8, 4, FAKE, kvw.DTYPE_F32, 64, FAKE,
+            kvw.DTYPE_BF16, ctypes.byref(c), 1, 1e-6, None, 0]
+    assert f(*args[:12], None, *args[13:]) == kvw.KVW_EINVAL  # no cache
+    a = list(args)
+    a[5] = 0
+    assert f(*a) == kvw.KVW_OK  # no tokens
+    a = list(args)
+    a[0] = ODD
+    assert f(*a) == kvw.KVW_EINVAL
+    c2 = _mla_cache(scale=-1.0)
+    a = list(args)
+    a[12] = ctypes.byref(c2)
+    assert f(*a) == kvw.KVW_EINVAL
+
+
+def test_gather_host_checks():
+    c = _mla_cache()
+    f = kvw.lib.kvw_mla_gather_latent
+    assert f(FAKE, kvw.DTYPE_BF16, 1.0, ctypes.byref(c), 1, FAKE, 2, 0, None, 0) == kvw.KVW_OK
+    assert f(FAKE, kvw.DTYPE_F32, 1.0, ctypes.byref(c), 1, FAKE, 2, 8, None, 0) == \
+        kvw.KVW_EUNSUPPORTED
+    assert f(ODD, kvw.DTYPE_BF16, 1.0, ctypes.byref(c), 1, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    assert f(FAKE, kvw.DTYPE_FP8_E4M3, 0.0, ctypes.byref(c), 1, FAKE, 2, 8, None, 0) == \
+        kvw.KVW_EINVAL
+    assert f(FAKE, kvw.DTYPE_BF16, 1.0, ctypes.byref(c), 2, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    c2 = _mla_cache(head_size=512)
+    assert f(FAKE, kvw.DTYPE_BF16, 1.0, ctypes.byref(c2), 1, FAKE, 2, 8, None, 0) == \
+        kvw.KVW_EUNSUPPORTED
+
+
+def test_codec_host_checks():
+    conv = kvw.lib.kvw_convert_bf16_to_fp8_e4m3
+    assert conv(FAKE, FAKE, 0, 1.0, 0) == kvw.KVW_OK
+    assert conv(FAKE, FAKE, 12, 1.0, 0) == kvw.KVW_EINVAL  # not a multiple of 8
+    assert conv(FAKE, ODD, 16, 1.0, 0) == kvw.KVW_EINVAL
+    assert conv(FAKE, FAKE, 16, 0.0, 0) == kvw.KVW_EINVAL
+    q = kvw.lib.kvw_quantize_fp8_rows
+    assert q(FAKE, FAKE, FAKE, 0, 64, 64, 64, 0) == kvw.KVW_OK
+    assert q(FAKE, FAKE, FAKE, 4, 60, 64, 64, 0) == kvw.KVW_EINVAL
+    assert q(FAKE, FAKE, FAKE, 4, 64, 60, 64, 0) == kvw.KVW_EINVAL
+    assert q(FAKE, FAKE, ODD, 4, 64, 64, 64, 0) == kvw.KVW_EINVAL

@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 from gqa_kv_cache_mla_gb300 import workloads as W
-from helpers import compare_bf16, compare_cache, expected_slots
+from helpers import compare_bf16, compare_cache, compare_e4m3, expected_slots
 
 pytestmark = pytest.mark.gpu
 
@@ -42,12 +42,16 @@ def run_mla(orc, dev, w, **kw):
     import torch
 
     torch.cuda.synchronize()
-    q_ref, c_ref, f_ref = orc.mla_rope_rmsnorm_quant(w, q_rope_out=d.q_out_init.copy(),
-                                                     nthreads=NTHREADS)
+    fn = orc.mla_rope_rmsnorm_inplace if w.inplace else orc.mla_rope_rmsnorm_quant
+    q_ref, c_ref, f_ref = fn(w, q_rope_out=d.q_out_init.copy(), nthreads=NTHREADS,
+                             out_dtype=w.q_out_dtype)
     assert d.guards_intact()
     assert d.flags() == f_ref
     c = w.cache
-    nq = compare_bf16(d.q_out.host(), q_ref)
+    if w.q_out_dtype == W.DTYPE_BF16:
+        nq = compare_bf16(d.q_out.host(), q_ref)
+    else:
+        nq = compare_e4m3(d.q_out.host(), q_ref)
     slots = [] if f_ref & 4 else expected_slots(w.offsets, c.cache_lengths, c.page_table,
                                                 c.page_size, c.num_pages)
     nc = compare_cache(c, d.cache.host(), c_ref, slots, w.layer_idx,
@@ -384,3 +388,149 @@ def test_max_batches_all_entry_points(orc, dev):
 def test_knorm_variant_configs_full(orc, dev, name):
     w = W.REGISTRY[name][0](2)
     run_knorm(orc, dev, w, per_head_norm=w.per_head_norm)
+
+
+
+# ------------------------------------------------------------ FP8 q output, in-place variant
+
+@pytest.mark.parametrize("build", ["tiny", "decode", "prefill"])
+def test_mla_fp8_q_output(orc, dev, build):
+    import dataclasses
+
+    w = {"tiny": lambda: W.mla_tiny(W.DTYPE_FP8_E4M3), "decode": lambda: W.mla_decode(),
+         "prefill": lambda: W.mla_prefill(W.DTYPE_FP8_E4M3)}[build]()
+    run_mla(orc, dev, dataclasses.replace(w, q_out_dtype=W.DTYPE_FP8_E4M3))
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_BF16, W.DTYPE_FP8_E4M3])
+@pytest.mark.parametrize("build", ["tiny", "decode", "prefill", "odd"])
+def test_mla_inplace(orc, dev, dtype, build):
+    if build == "tiny":
+        w = W.mla_tiny(dtype)
+    elif build == "decode":
+        w = W.mla_decode(dtype)
+    elif build == "prefill":
+        w = W.mla_prefill(dtype)
+    else:  # stream path, odd head counts, empty requests, a second layer, scale 2
+        rng = np.random.default_rng(820)
+        new = rng.integers(300, 3000, 7)
+        new[3] = 0
+        w = W.mla_workload("ip", 821, new, rng.integers(0, 2000, 7), num_heads=3, page_size=64,
+                           max_seq_len=8192, cache_dtype=dtype, num_layers=2, layer_idx=1,
+                           scale=2.0)
+    run_mla(orc, dev, W.mla_inplace(w))
+
+
+def test_mla_inplace_flags(orc, dev):
+    w = W.mla_workload("pf", 91, [2, 5], [0, 60], num_heads=2, page_size=16, max_seq_len=80,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    w.freqs = w.freqs[:64].copy()
+    w = W.mla_inplace(w)
+    w.cache.page_table[0, 0] = W.PAGE_UNMAPPED
+    d, _, _ = run_mla(orc, dev, w)
+    assert d.flags() == 3
+
+
+# ------------------------------------------------------------ paged -> contiguous gather
+
+def run_gather(orc, dev, g):
+    import torch
+
+    d = dev.DeviceGather(g)
+    d.run()
+    torch.cuda.synchronize()
+    ref, f_ref = orc.mla_gather_latent(g.cache, g.layer_idx, g.ctx_offsets, g.out_dtype,
+                                       g.out_scale, out=d.out_init.copy())
+    assert d.guards_intact()
+    assert d.flags() == f_ref
+    got = d.out.host()
+    if g.out_dtype == W.DTYPE_BF16:
+        assert np.array_equal(got, ref)  # a copy or an exact E4M3 -> bf16 widening
+    else:
+        compare_e4m3(got, ref)
+    assert np.array_equal(d.cache.host(), g.cache.data)  # the cache is only read
+    return d
+
+
+@pytest.mark.parametrize("src", [W.DTYPE_BF16, W.DTYPE_FP8_E4M3])
+@pytest.mark.parametrize("dst", [W.DTYPE_BF16, W.DTYPE_FP8_E4M3])
+def test_gather_small(orc, dev, src, dst):
+    w = W.mla_workload("g", 830, [3, 0, 17, 1, 40], [5, 9, 100, 31, 0], num_heads=1,
+                       page_size=16, max_seq_len=256, cache_dtype=src, num_layers=2, layer_idx=1,
+                       scale=0.5)
+    run_gather(orc, dev, W.mla_gather(w, out_dtype=dst, out_scale=2.0))
+
+
+@pytest.mark.parametrize("dst", [W.DTYPE_FP8_E4M3, W.DTYPE_BF16])
+def test_gather_prefill_full(orc, dev, dst):
+    run_gather(orc, dev, W.mla_gather(W.mla_prefill(W.DTYPE_BF16), out_dtype=dst))
+
+
+def test_gather_decode_contexts(orc, dev):
+    run_gather(orc, dev, W.mla_gather(W.mla_decode(W.DTYPE_FP8_E4M3), out_dtype=W.DTYPE_BF16))
+
+
+def test_gather_flags(orc, dev):
+    w = W.mla_workload("g", 831, [3, 5], [0, 7], num_heads=1, page_size=16, max_seq_len=64,
+                       cache_dtype=W.DTYPE_BF16)
+    g = W.mla_gather(w)
+    g.cache.page_table[1, 0] = W.PAGE_UNMAPPED
+    assert run_gather(orc, dev, g).flags() == 1
+    g = W.mla_gather(W.mla_workload("g", 832, [3, 5], [0, 7], num_heads=1, page_size=16,
+                                    max_seq_len=64, cache_dtype=W.DTYPE_BF16))
+    g.ctx_offsets = g.ctx_offsets.copy()
+    g.ctx_offsets[1] = g.ctx_offsets[2] + 1  # decreasing
+    assert run_gather(orc, dev, g).flags() == 4
+
+
+# ------------------------------------------------------------ FP8 codecs
+
+def test_convert_all_bf16_patterns_and_random(orc, dev):
+    import torch
+
+    from gqa_kv_cache_mla_gb300 import kvw
+
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = (h.astype(np.uint32) << 16).view(np.float32)
+    h = h[np.isfinite(v)]
+    h = h[: h.size // 8 * 8]
+    rng = np.random.default_rng(840)
+    x = np.concatenate([h, W.normal_bf16(rng, (1 << 20,), std=3.0)])
+    for scale in (1.0, 0.37):
+        d = dev.Guarded(x, "cuda")
+        out = dev.Guarded(np.zeros(x.size, np.uint8), "cuda")
+        kvw.kvw_convert_bf16_to_fp8_e4m3(out.tensor, d.tensor, scale)
+        torch.cuda.synchronize()
+        assert out.guards_intact() and d.guards_intact()
+        assert np.array_equal(out.host(), orc.convert_bf16_to_e4m3(x, scale))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (37, 576), (4096, 2048)])
+def test_quantize_rows(orc, dev, rows, cols):
+    import torch
+
+    from gqa_kv_cache_mla_gb300 import kvw
+
+    rng = np.random.default_rng(841 + rows)
+    x = W.normal_bf16(rng, (rows, cols), outlier_frac=0.01)
+    x[0, :] = 0  # an all-zero row: scale 1
+    d = dev.Guarded(x, "cuda")
+    out = dev.Guarded(np.zeros(x.shape, np.uint8), "cuda")
+    sc = dev.Guarded(np.zeros(rows, np.float32), "cuda")
+    kvw.kvw_quantize_fp8_rows(out.tensor, sc.tensor, d.tensor)
+    torch.cuda.synchronize()
+    assert out.guards_intact() and sc.guards_intact()
+    codes, scales = orc.quantize_rows_e4m3(x)
+    assert np.array_equal(sc.host(), scales)
+    assert np.array_equal(out.host(), codes)
+
+
+def test_quantize_rows_benchmark_shape(orc, dev):
+    import torch
+
+    w = W.fp8_quant_rows()
+    d = dev.DeviceConvert(w)
+    d.run()
+    torch.cuda.synchronize()
+    codes, scales = orc.quantize_rows_e4m3(w.x)
+    assert np.array_equal(d.scales.host(), scales) and np.array_equal(d.out.host(), codes)
