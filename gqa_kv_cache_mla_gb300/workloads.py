@@ -560,6 +560,11 @@ REGISTRY = {
     "mla_prefill_bf16_4req": (lambda s: mla_prefill(DTYPE_BF16, seed=s + 1, num_requests=4),
                               "mla_rope_rmsnorm_quant.cu",
                               "MLA ragged prefill, 4 of the 16 requests (profiling size), bf16 cache"),
+    "mla_prefill_inplace_4req": (lambda s: mla_inplace(mla_prefill(DTYPE_BF16, seed=s + 1,
+                                                                    num_requests=4)),
+                                 "mla_rope_rmsnorm_quant.cu",
+                                 "MLA ragged prefill in place, 4 of the 16 requests (profiling "
+                                 "size), bf16 cache"),
     "gqa_interleaved": (lambda s: gqa_llama3(True, None, seed=s + 2), "qk_rope_paged_ragged.cu",
                         "GQA Llama-3-8B Q/K RoPE, interleaved, slot positions"),
     "gqa_half_ids": (lambda s: gqa_llama3(False, "ids", seed=s + 2), "qk_rope_paged_ragged.cu",
