@@ -56,12 +56,15 @@ def written_row_mask(cache, slots, layer_idx):
     return m
 
 
-def compare_cache(cache, gpu, ref, slots, layer_idx, fp8, max_ulp_frac=None, cols=None):
+def compare_cache(cache, gpu, ref, slots, layer_idx, fp8, max_ulp_frac=None, cols=None,
+                  bf16_max_ulp=1):
     """GPU cache vs oracle cache.
 
     Elements outside the rows the call writes (and, with ``cols``, columns at
     or past ``cols``) must be bit-identical; inside, bf16 may differ by 1 ulp
     and FP8 by 1 ulp on at most ``max_ulp_frac`` of the written elements.
+    ``bf16_max_ulp`` > 1 (for results rounded twice) allows differences up to
+    that many ulp on at most 1e-3 of the written elements.
     Returns the number of differing elements.
     """
     gpu = gpu.reshape(-1)
@@ -92,7 +95,10 @@ def compare_cache(cache, gpu, ref, slots, layer_idx, fp8, max_ulp_frac=None, col
         assert frac <= (max_ulp_frac if max_ulp_frac is not None else 1e-3), frac
     else:
         u = bf16_ulp_diff(gpu[diff], ref[diff])
-        assert u.max() <= 1, "bf16 difference above 1 ulp: %d" % int(u.max())
+        assert u.max() <= bf16_max_ulp, "bf16 difference above %d ulp: %d" % (bf16_max_ulp,
+                                                                             int(u.max()))
+        n_written = len(slots) * cache.num_heads * (cols or cache.head_size)
+        assert (u > 1).sum() <= max(1.0, 1e-3 * n_written), int((u > 1).sum())
     return int(diff.size)
 
 
@@ -103,7 +109,10 @@ def compare_bf16(gpu, ref):
     diff = np.flatnonzero(gpu != ref)
     if diff.size:
         u = bf16_ulp_diff(gpu[diff], ref[diff])
-        assert u.max() <= 1, "bf16 difference above 1 ulp: %d" % int(u.max())
+        assert u.max() <= bf16_max_ulp, "bf16 difference above %d ulp: %d" % (bf16_max_ulp,
+                                                                             int(u.max()))
+        n_written = len(slots) * cache.num_heads * (cols or cache.head_size)
+        assert (u > 1).sum() <= max(1.0, 1e-3 * n_written), int((u > 1).sum())
     return int(diff.size)
 
 
