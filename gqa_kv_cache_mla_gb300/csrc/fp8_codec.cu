@@ -7,9 +7,27 @@
 //
 // GB300 design: HBM streaming.  The conversion moves 16 bytes in and 8 bytes
 // out per thread and iteration (grid-stride, 4 iterations in flight).  The
-// per-row quantiser gives each row to one warp: a first pass over the row
-// finds max|x| (16-byte loads, warp max-reduction), the second pass re-reads
-// the row (now in L1/L2) and writes the codes; the scale is stored per row.
+// per-row quantiser gives each row to one warp.  Rows of up to 2048 values
+// are held in registers (one 16-byte load per lane and 256 columns, all
+// issued before any use), so the row is read from HBM once: warp
+// max-reduction of |x|, the scale, then the codes from the registers.  Longer
+// rows take a two-pass loop (the second pass re-reads the row from L1/L2).
+//
+// The per-element division x / scale is the costly part of the quantiser
+// (an IEEE divide per value made the first version instruction-bound).  It
+// is replaced by one multiply by y = RN(1/scale) and one FMA correction step
+// (Markstein's division refinement: P. Markstein, IBM J. Res. Dev. 34(1),
+// 1990; also the FMA-based division chapter of Muller et al., Handbook of
+// Floating-Point Arithmetic): q0 = RN(x*y), r = x - q0*scale (exact with an
+// FMA), q = RN(q0 + r*y), which is the correctly rounded quotient while
+// scale, 1/scale and the remainder are normal numbers.  Here x is a bf16
+// value and scale = RN(amax / 448) with amax a bf16 magnitude; the path is
+// taken for scales in [2^-60, 2^60], where every quotient of magnitude
+// >= 2^-14 keeps all three normal, and smaller quotients give an E4M3 zero
+// of the right sign whatever their last bits.  Other scales use the IEEE
+// divide.  The tests compare every code with a plain division in the CPU
+// reference, on rows that hold every bf16 mantissa at every binade that
+// matters against every scale mantissa this path can meet.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -41,6 +59,71 @@ __global__ void __launch_bounds__(kThreads) convert_kernel(uint2* out, const uin
     }
 }
 
+// x / s for the quantiser, from y = RN(1/s): see the file comment for the
+// method and its range.  copysignf keeps the sign of x on a zero result.
+__device__ __forceinline__ float div_refined(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, s, x);
+    return copysignf(__fmaf_rn(r, y, q0), x);
+}
+
+// Scale of a row: max|x| / 448, or 1 for a row of zeros.
+__device__ __forceinline__ float row_scale(float amax) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+__device__ __forceinline__ bool refined_ok(float sc) { return sc >= 0x1p-60f && sc <= 0x1p60f; }
+
+template <bool REFINED>
+__device__ __forceinline__ uint2 quantize8(const uint4& v, float sc, float y) {
+    float f[8];
+    unpack8(v, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = REFINED ? div_refined(f[e], sc, y) : __fdiv_rn(f[e], sc);
+    return pack8_e4m3(f);
+}
+
+// One warp per row, VPL 16-byte vectors per lane held in registers
+// (cols <= 256 * VPL).
+template <int VPL>
+__global__ void __launch_bounds__(kThreads) quantize_rows_reg_kernel(
+    unsigned char* out, float* scales, const uint16_t* in, uint32_t rows, uint32_t cols,
+    int64_t in_stride, int64_t out_stride) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t r = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const uint4* row = reinterpret_cast<const uint4*>(in + (int64_t)r * in_stride);
+    const uint32_t nvec = cols / 8;
+    uint4 v[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k)
+        v[k] = lane + 32u * k < nvec ? ld_stream(row + lane + 32u * k) : make_uint4(0, 0, 0, 0);
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+        float f[8];
+        unpack8(v[k], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+    }
+    const float sc = row_scale(amax);
+    if (lane == 0) scales[r] = sc;
+    uint2* orow = reinterpret_cast<uint2*>(out + (int64_t)r * out_stride);
+    if (refined_ok(sc)) {
+        const float y = __frcp_rn(sc);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+            if (lane + 32u * k < nvec) orow[lane + 32u * k] = quantize8<true>(v[k], sc, y);
+    } else {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+            if (lane + 32u * k < nvec) orow[lane + 32u * k] = quantize8<false>(v[k], sc, 0.0f);
+    }
+}
+
+// Rows longer than 2048 values: max pass, then a second pass over the row.
 __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(unsigned char* out, float* scales,
                                                                  const uint16_t* in, uint32_t rows,
                                                                  uint32_t cols, int64_t in_stride,
@@ -57,15 +140,15 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(unsigned char* 
 #pragma unroll
         for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float sc = row_scale(amax);
     if (lane == 0) scales[r] = sc;
-    unsigned char* orow = out + (int64_t)r * out_stride;
-    for (uint32_t v = lane; v < nvec; v += 32) {
-        float f[8];
-        unpack8(ld_stream(row + v), f);
-        store_k8<true>(orow + 8 * v, f, sc);
+    uint2* orow = reinterpret_cast<uint2*>(out + (int64_t)r * out_stride);
+    if (refined_ok(sc)) {
+        const float y = __frcp_rn(sc);
+        for (uint32_t v = lane; v < nvec; v += 32) orow[v] = quantize8<true>(ld_stream(row + v), sc, y);
+    } else {
+        for (uint32_t v = lane; v < nvec; v += 32)
+            orow[v] = quantize8<false>(ld_stream(row + v), sc, 0.0f);
     }
 }
 
@@ -108,8 +191,24 @@ extern "C" int kvw_quantize_fp8_rows(void* out_codes, float* out_scales, const v
         (reinterpret_cast<uintptr_t>(out_scales) & 3u) != 0)
         return KVW_EINVAL;
     const uint32_t rows_per_cta = kThreads / 32;
-    quantize_rows_kernel<<<(rows + rows_per_cta - 1) / rows_per_cta, kThreads, 0, stream>>>(
-        static_cast<unsigned char*>(out_codes), out_scales, static_cast<const uint16_t*>(in), rows,
-        cols, in_row_stride, out_row_stride);
+    const uint32_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
+    auto o = static_cast<unsigned char*>(out_codes);
+    auto x = static_cast<const uint16_t*>(in);
+    const uint32_t vpl = (cols + 255) / 256;  // 16-byte vectors per lane
+    if (vpl <= 1)
+        quantize_rows_reg_kernel<1><<<grid, kThreads, 0, stream>>>(o, out_scales, x, rows, cols,
+                                                                  in_row_stride, out_row_stride);
+    else if (vpl <= 2)
+        quantize_rows_reg_kernel<2><<<grid, kThreads, 0, stream>>>(o, out_scales, x, rows, cols,
+                                                                  in_row_stride, out_row_stride);
+    else if (vpl <= 4)
+        quantize_rows_reg_kernel<4><<<grid, kThreads, 0, stream>>>(o, out_scales, x, rows, cols,
+                                                                  in_row_stride, out_row_stride);
+    else if (vpl <= 8)
+        quantize_rows_reg_kernel<8><<<grid, kThreads, 0, stream>>>(o, out_scales, x, rows, cols,
+                                                                  in_row_stride, out_row_stride);
+    else
+        quantize_rows_kernel<<<grid, kThreads, 0, stream>>>(o, out_scales, x, rows, cols,
+                                                           in_row_stride, out_row_stride);
     return cudaGetLastError() == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }

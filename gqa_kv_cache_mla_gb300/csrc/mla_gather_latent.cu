@@ -5,11 +5,17 @@
 // contiguous buffer and quantises them ("mla_graph" module page, entry
 // mla_prefill_branch_fp8; the copy feeds the K/V up-projection GEMMs).
 //
-// GB300 design: pure streaming.  One warp per output row (576 values): the
-// row's request comes from a binary search over the context offsets staged in
-// shared memory, its page from the page table; lanes move 16-byte (bf16) or
-// 8-byte (E4M3) pieces, convert in registers and store.  Each warp handles
-// kRowsPerWarp rows with all loads issued before any store.
+// GB300 design: pure streaming with persistent CTAs (one wave, the occupancy
+// the register count allows).  A CTA stages the context offsets once, then
+// walks tiles of kTileRows consecutive output rows.  A tile is 32 x 72
+// pieces of 8 values; each of the 256 threads moves the same 9 pieces of
+// every tile (fixed row and column slots), so all lanes stay busy and the 9
+// loads of a thread are in flight together.  The cache address of each row
+// of a tile (request by binary search over the staged offsets, page from the
+// page table) is resolved by the first 32 threads one tile ahead, into the
+// other half of a double-buffered shared array, while the current tile's
+// loads are in flight; consecutive rows of one page are adjacent in memory,
+// so a tile's loads are mostly one contiguous run.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -18,8 +24,11 @@ namespace kvw {
 namespace {
 
 constexpr uint32_t kThreads = 256;
-constexpr uint32_t kRowsPerWarp = 4;
 constexpr uint32_t kRow = 576;
+constexpr uint32_t kPiecesPerRow = kRow / 8;                                 // 72
+constexpr uint32_t kTileRows = 32;
+constexpr uint32_t kPiecesPerThread = kTileRows * kPiecesPerRow / kThreads;  // 9
+static_assert(kTileRows * kPiecesPerRow == kPiecesPerThread * kThreads, "tile shape");
 
 struct GatherArgs {
     unsigned char* out;
@@ -32,15 +41,15 @@ struct GatherArgs {
     float cache_scale, out_scale;
 };
 
-// Raw bytes of 8 cache elements starting at element `col` (16 bytes of bf16
-// or 8 bytes of E4M3, kept in .x/.y).
+// Raw bytes of 8 cache elements at element offset `e` (16 bytes of bf16 or
+// 8 bytes of E4M3, kept in .x/.y).
 template <bool CF8>
-__device__ __forceinline__ uint4 load_raw8(const GatherArgs& a, int64_t base, uint32_t col) {
+__device__ __forceinline__ uint4 load_raw8(const unsigned char* cache, int64_t e) {
     if (CF8) {
-        const uint2 v = *reinterpret_cast<const uint2*>(a.cache + base + col);
+        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(cache + e));
         return make_uint4(v.x, v.y, 0, 0);
     }
-    return *reinterpret_cast<const uint4*>(a.cache + (base + col) * 2);
+    return ld_stream(reinterpret_cast<const uint4*>(cache + e * 2));
 }
 
 // Raw cache elements -> fp32 values (E4M3 times the cache scale).
@@ -57,8 +66,26 @@ __device__ __forceinline__ void to_f32(const uint4& raw, float scale, float (&f)
     }
 }
 
+// Cache element offset of output row r (or -1: no valid page, flagged).
+__device__ __forceinline__ int64_t row_base(const GatherArgs& a, const uint32_t* s_off,
+                                            uint32_t r) {
+    if (r >= a.rows) return -1;
+    const uint32_t b = find_request(s_off, a.B, r);
+    const uint32_t pos = r - s_off[b];
+    const uint32_t pidx = pos / a.page_size;
+    const uint32_t page = pidx < a.max_pages
+                              ? __ldg(a.page_table + (uint64_t)b * a.max_pages + pidx)
+                              : KVW_PAGE_UNMAPPED;
+    if (page >= a.num_pages) {
+        flag(a.err_flags, KVW_ERR_PAGE);
+        return -1;
+    }
+    return (int64_t)page * a.s_page + a.layer_off + (int64_t)(pos - pidx * a.page_size) * a.s_token;
+}
+
 template <bool CF8, bool OF8>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherArgs a) {
+    __shared__ int64_t s_base[2][kTileRows];
     extern __shared__ uint32_t s_off[];
     int ok = 1;
     for (uint32_t i = threadIdx.x; i <= a.B; i += blockDim.x) {
@@ -71,47 +98,39 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t warp_global = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    const uint32_t r0 = warp_global * kRowsPerWarp;
-    // lane l owns columns 8l..8l+7, 256+8l.., and (l < 8) 512+8l..
-    int64_t base[kRowsPerWarp];
-    uint4 raw[kRowsPerWarp][3];
+    const uint32_t tiles = (a.rows + kTileRows - 1) / kTileRows;
+    uint32_t tile = blockIdx.x;
+    if (tile >= tiles) return;
+    if (threadIdx.x < kTileRows) s_base[0][threadIdx.x] = row_base(a, s_off, tile * kTileRows + threadIdx.x);
+    __syncthreads();
+    // this thread's fixed pieces: (row slot, column) of piece threadIdx.x + k * kThreads
+    uint32_t prow[kPiecesPerThread], pcol[kPiecesPerThread];
 #pragma unroll
-    for (uint32_t q = 0; q < kRowsPerWarp; ++q) {
-        const uint32_t r = r0 + q;
-        base[q] = -1;
-        if (r < a.rows) {
-            const uint32_t b = find_request(s_off, a.B, r);
-            const uint32_t pos = r - s_off[b];
-            const uint32_t pidx = pos / a.page_size;
-            const uint32_t page =
-                pidx < a.max_pages ? __ldg(a.page_table + (uint64_t)b * a.max_pages + pidx)
-                                   : KVW_PAGE_UNMAPPED;
-            if (page < a.num_pages)
-                base[q] = (int64_t)page * a.s_page + a.layer_off +
-                          (int64_t)(pos - pidx * a.page_size) * a.s_token;
-            else if (lane == 0)
-                flag(a.err_flags, KVW_ERR_PAGE);
-        }
-        if (base[q] >= 0) {
-            raw[q][0] = load_raw8<CF8>(a, base[q], lane * 8);
-            raw[q][1] = load_raw8<CF8>(a, base[q], 256 + lane * 8);
-            if (lane < 8) raw[q][2] = load_raw8<CF8>(a, base[q], 512 + lane * 8);
-        }
+    for (uint32_t k = 0; k < kPiecesPerThread; ++k) {
+        const uint32_t p = threadIdx.x + k * kThreads;
+        prow[k] = p / kPiecesPerRow;
+        pcol[k] = (p % kPiecesPerRow) * 8;
     }
+    uint32_t buf = 0;
+    for (; tile < tiles; tile += gridDim.x, buf ^= 1u) {
+        uint4 raw[kPiecesPerThread];
 #pragma unroll
-    for (uint32_t q = 0; q < kRowsPerWarp; ++q) {
-        if (base[q] < 0) continue;
-        unsigned char* orow = a.out + (uint64_t)(r0 + q) * kRow * (OF8 ? 1 : 2);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            if (j == 2 && lane >= 8) break;
-            const uint32_t col = 256u * j + lane * 8;
-            float v[8];
-            to_f32<CF8>(raw[q][j], a.cache_scale, v);
-            store_k8<OF8>(orow + col * (OF8 ? 1 : 2), v, a.out_scale);
+        for (uint32_t k = 0; k < kPiecesPerThread; ++k) {
+            const int64_t base = s_base[buf][prow[k]];
+            if (base >= 0) raw[k] = load_raw8<CF8>(a.cache, base + pcol[k]);
         }
+        const uint32_t next = tile + gridDim.x;
+        if (next < tiles && threadIdx.x < kTileRows)
+            s_base[buf ^ 1u][threadIdx.x] = row_base(a, s_off, next * kTileRows + threadIdx.x);
+#pragma unroll
+        for (uint32_t k = 0; k < kPiecesPerThread; ++k) {
+            if (s_base[buf][prow[k]] < 0) continue;
+            float v[8];
+            to_f32<CF8>(raw[k], a.cache_scale, v);
+            const uint64_t e = (uint64_t)(tile * kTileRows + prow[k]) * kRow + pcol[k];
+            store_k8<OF8>(a.out + e * (OF8 ? 1 : 2), v, a.out_scale);
+        }
+        __syncthreads();  // next tile's bases visible; this tile's no longer read
     }
 }
 
@@ -123,8 +142,14 @@ cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const uint32_t rows_per_cta = (kThreads / 32) * kRowsPerWarp;
-    k<<<(a.rows + rows_per_cta - 1) / rows_per_cta, kThreads, smem, stream>>>(a);
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const uint32_t tiles = (a.rows + kTileRows - 1) / kTileRows;
+    const uint32_t wave = (uint32_t)(sms * (per_sm > 0 ? per_sm : 1));
+    k<<<tiles < wave ? tiles : wave, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -538,6 +538,62 @@ def test_quantize_rows(orc, dev, rows, cols):
     assert np.array_equal(out.host(), codes)
 
 
+def quant_rows_mantissa_sweep(shift):
+    """Rows for the per-row quantiser that meet every scale mantissa it can see
+    with every bf16 value whose quotient can give a non-zero code.
+
+    Up to a power of two, the row maximum a is one of 128 bf16 values in
+    [1, 2), so scale = RN(a / 448) takes 128 mantissas.  For each a, the row
+    group holds a itself and every bf16 x of either sign with
+    2^-23 <= |x| <= a (quotients down to about 2^-14), plus zeros of both
+    signs and a few subnormals; the whole group is then shifted by 2^shift
+    (exponent field + shift) to reach other scale binades."""
+    groups = []
+    exps = np.arange(127 - 23, 128, dtype=np.uint16)
+    allx = ((exps[:, None] << 7) | np.arange(128, dtype=np.uint16)[None, :]).reshape(-1)
+    for ma in range(128):
+        a = np.uint16(0x3F80 | ma)
+        xs = allx[allx <= a]
+        vals = np.concatenate([xs, xs | 0x8000]).astype(np.uint16)
+        if shift:
+            vals = (vals.astype(np.int32) + (shift << 7)).astype(np.uint16)
+        a_s = np.uint16(int(a) + (shift << 7))
+        extra = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F], np.uint16)
+        vals = np.concatenate([vals, extra])
+        per_row = 2047
+        n_rows = -(-vals.size // per_row)
+        block = np.zeros((n_rows, 2048), np.uint16)
+        block[:, 0] = a_s
+        flat = np.zeros(n_rows * per_row, np.uint16)
+        flat[: vals.size] = vals
+        block[:, 1:] = flat.reshape(n_rows, per_row)
+        groups.append(block)
+    return np.concatenate(groups)
+
+
+@pytest.mark.parametrize("shift", [0, 40, -40, -80, 100])
+def test_quantize_rows_every_scale_mantissa(orc, dev, shift):
+    """Bit-exact codes and scales on the mantissa sweep: shifts 0 and +-40 use
+    the reciprocal-and-FMA division, -80 and +100 (scales outside [2^-60,
+    2^60]) the IEEE divide."""
+    import torch
+
+    from gqa_kv_cache_mla_gb300 import kvw
+
+    x = quant_rows_mantissa_sweep(shift)
+    d = dev.Guarded(x, "cuda")
+    out = dev.Guarded(np.zeros(x.shape, np.uint8), "cuda")
+    sc = dev.Guarded(np.zeros(x.shape[0], np.float32), "cuda")
+    kvw.kvw_quantize_fp8_rows(out.tensor, sc.tensor, d.tensor)
+    torch.cuda.synchronize()
+    codes, scales = orc.quantize_rows_e4m3(x)
+    assert np.array_equal(sc.host(), scales)
+    got = out.host()
+    bad = np.flatnonzero(got != codes)
+    assert bad.size == 0, (bad.size, x.reshape(-1)[bad[:5]], got.reshape(-1)[bad[:5]],
+                           codes.reshape(-1)[bad[:5]])
+
+
 def test_quantize_rows_benchmark_shape(orc, dev):
     import torch
 
