@@ -12,10 +12,14 @@
 // vectors l, l + TL, ... of it, sums its squares, and an xor-shuffle inside
 // the team finishes the reduction, so no shared memory or block barrier is
 // needed for the norm itself.  Each team handles RPT rows so every thread has
-// RPT x VPL 16-byte loads in flight.  The CTA first resolves the page slot of
-// the few tokens its rows belong to (ragged lookup in shared memory), then
-// reads, normalises and writes back in place.  Columns at or past gamma_len
-// are neither read into the sum nor written.
+// RPT x VPL 16-byte loads in flight.  CTAs are persistent (one wave at the
+// occupancy the register count allows): a CTA stages the ragged tables once,
+// then walks tiles of rows_per_block rows.  The page slots of the few tokens
+// of the next tile are resolved (ragged lookup in shared memory, page table)
+// while the current tile's loads are in flight, into the other half of a
+// double-buffered shared array; then the tile is normalised and written back
+// in place.  Columns at or past gamma_len are neither read into the sum nor
+// written.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -25,6 +29,7 @@ namespace {
 
 constexpr uint32_t kThreads = 256;
 constexpr uint32_t kMaxCols = 2048;
+constexpr uint32_t kMaxTileTokens = kThreads * 2 + 2;  // tokens of up to 512 rows
 
 struct KnArgs {
     uint16_t* cache;
@@ -49,57 +54,53 @@ struct KnArgs {
 // vector).  Both are template parameters so the per-element inner loops are
 // branch-free: unpack, square-and-add, scale, weight, pack.
 template <int VPL, int RPT, bool MBC, bool FULL>
-__global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a) {
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
     uint32_t* s_clen = s_dyn + a.B + 1;
-    __shared__ int64_t s_base[kThreads * 2 + 2];  // tokens of up to 512 rows
+    __shared__ int64_t s_base[2][kMaxTileTokens];
 
     const uint32_t TL = 1u << a.tl_log2;
     const uint32_t team = threadIdx.x >> a.tl_log2;
     const uint32_t tl = threadIdx.x & (TL - 1u);
     const uint32_t teams = kThreads >> a.tl_log2;
-    const uint32_t r0 = blockIdx.x * a.rows_per_block;
-    const uint32_t t_lo = r0 / a.rows_per_token;
 
-    // weights of this lane's columns (the same for every row)
-    float w[VPL][8];
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-        const uint32_t c = (tl + v * TL) * 8u;
-        if (FULL) {
-            if (c < a.G) {
-                float g[8];
-                unpack8(ld_table(reinterpret_cast<const uint4*>(a.gamma + c)), g);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[v][e] = __fadd_rn(g[e], a.wo);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[v][e] = 0.0f;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                w[v][e] = (c + e < a.G) ? __fadd_rn(bf16_lo(a.gamma[c + e]), a.wo) : 0.0f;
-        }
-    }
+    // weights gamma + weight_offset of the normalised columns, in shared memory
+    // (zero past gamma_len), read as float4 pairs by the lanes of each column
+    __shared__ __align__(16) float s_w[kMaxCols];
+    const uint32_t gcols = a.nv * 8u;
+    for (uint32_t c = threadIdx.x; c < gcols; c += kThreads)
+        s_w[c] = c < a.G ? __fadd_rn(bf16_lo(__ldg(a.gamma + c)), a.wo) : 0.0f;
 
     if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-    const uint32_t r_end = min(r0 + a.rows_per_block, a.rows);
-    const uint32_t t_hi = (r_end - 1) / a.rows_per_token;
-    for (uint32_t k = threadIdx.x; k <= t_hi - t_lo; k += kThreads) {
-        const uint32_t t = t_lo + k;
-        const uint32_t b = find_request(s_off, a.B, t);
-        const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-        const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
-                                      a.s_token, a.layer_off, b, pos);
-        s_base[k] = base;
-        if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
-    }
+    const uint32_t tiles = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
+    uint32_t tile = blockIdx.x;
+    if (tile >= tiles) return;
+    // page slot of every token of a tile -> dst[token - first token of the tile]
+    auto resolve = [&](uint32_t tl_idx, int64_t* dst) {
+        const uint32_t r0 = tl_idx * a.rows_per_block;
+        const uint32_t t_lo = r0 / a.rows_per_token;
+        const uint32_t t_hi = (min(r0 + a.rows_per_block, a.rows) - 1) / a.rows_per_token;
+        for (uint32_t k = threadIdx.x; k <= t_hi - t_lo; k += kThreads) {
+            const uint32_t t = t_lo + k;
+            const uint32_t b = find_request(s_off, a.B, t);
+            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+            const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size,
+                                          a.s_page, a.s_token, a.layer_off, b, pos);
+            dst[k] = base;
+            if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
+        }
+    };
+    resolve(tile, s_base[0]);
     __syncthreads();
+
+    for (uint32_t buf = 0; tile < tiles; tile += gridDim.x, buf ^= 1u) {
+    const uint32_t r0 = tile * a.rows_per_block;
+    const uint32_t t_lo = r0 / a.rows_per_token;
+    const uint32_t r_end = min(r0 + a.rows_per_block, a.rows);
 
     // pointers of this lane's first vector in each of its rows (null: no row);
     // row r = r0 + team + q * teams, walked as (token, head) without dividing
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
         const uint32_t r = r0 + team + q * teams;
         ptr[q] = nullptr;
         if (r < r_end) {
-            const int64_t base = s_base[t - t_lo];
+            const int64_t base = s_base[buf][t - t_lo];
             if (base >= 0) ptr[q] = a.cache + base + (a.per_head ? (int64_t)g * a.s_head : 0);
         }
         t += dt;
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
             }
         }
     }
+    if (tile + gridDim.x < tiles) resolve(tile + gridDim.x, s_base[buf ^ 1u]);
 
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
@@ -153,12 +155,15 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
         for (int v = 0; v < VPL; ++v) {
             const uint32_t c = (tl + v * TL) * 8u;
             if (c >= a.G) continue;
+            const float4 w0 = *reinterpret_cast<const float4*>(s_w + c);
+            const float4 w1 = *reinterpret_cast<const float4*>(s_w + c + 4);
+            const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
             float y[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float xr = __fmul_rn(xs[v][e], rinv);
-                y[e] = MBC ? __fmul_rn(xr, w[v][e])
-                           : __fmul_rn(__bfloat162float(__float2bfloat16_rn(xr)), w[v][e]);
+                y[e] = MBC ? __fmul_rn(xr, w[e])
+                           : __fmul_rn(__bfloat162float(__float2bfloat16_rn(xr)), w[e]);
             }
             const uint4 out = pack8_bf16(y);
             uint16_t* dst =
@@ -173,6 +178,8 @@ __global__ void __launch_bounds__(kThreads) rms_norm_kv_kernel(const KnArgs a) {
             }
         }
     }
+    __syncthreads();  // next tile's slots visible; this tile's no longer read
+    }
 }
 
 template <int VPL, int RPT, bool MBC, bool FULL>
@@ -182,8 +189,14 @@ cudaError_t launch_one(const KnArgs& a, size_t smem, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const uint32_t blocks = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
-    k<<<blocks, kThreads, smem, stream>>>(a);
+    const uint32_t tiles = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const uint32_t wave = (uint32_t)sms * (uint32_t)(per_sm > 0 ? per_sm : 1);
+    k<<<tiles < wave ? tiles : wave, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
