@@ -560,6 +560,9 @@ REGISTRY = {
     "mla_prefill_bf16_4req": (lambda s: mla_prefill(DTYPE_BF16, seed=s + 1, num_requests=4),
                               "mla_rope_rmsnorm_quant.cu",
                               "MLA ragged prefill, 4 of the 16 requests (profiling size), bf16 cache"),
+    "mla_prefill_fp8_4req": (lambda s: mla_prefill(DTYPE_FP8_E4M3, seed=s + 1, num_requests=4),
+                             "mla_rope_rmsnorm_quant.cu",
+                             "MLA ragged prefill, 4 of the 16 requests (profiling size), FP8 cache"),
     "mla_prefill_inplace_4req": (lambda s: mla_inplace(mla_prefill(DTYPE_BF16, seed=s + 1,
                                                                     num_requests=4)),
                                  "mla_rope_rmsnorm_quant.cu",
