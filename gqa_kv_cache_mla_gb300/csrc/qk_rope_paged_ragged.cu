@@ -656,12 +656,40 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return KVW_ECUDA;
     const uint64_t budget = (uint64_t)optin - 128 - tables - kStages * 1024;
-    uint64_t tpb = budget / (kStages * per_tok);
-    if (tpb > kMaxTPB) tpb = kMaxTPB;
+    uint64_t tpb_max = budget / (kStages * per_tok);
+    if (tpb_max > kMaxTPB) tpb_max = kMaxTPB;
     // small batches: spread the groups over all SMs
     const uint64_t spread = (tot_seq_len + (uint64_t)sms - 1) / sms;
-    if (tpb > spread) tpb = spread;
-    if (tpb == 0) return KVW_EUNSUPPORTED;
+    if (tpb_max > spread) tpb_max = spread;
+    if (tpb_max == 0) return KVW_EUNSUPPORTED;
+    // Tokens per group: the consumers split a group into tpb * G * slices
+    // units (one per thread), each rotating ceil(H / slices) heads.  The use
+    // of a split counts idle threads and the largest slice against the
+    // average one (for 40 heads of 128: 10 tokens x 3 slices use 0.89 of the
+    // consumers, 11 tokens x 2 slices 0.69).  Larger groups cost less
+    // producer work per token, so take the largest group whose use is at
+    // least 0.85, else the group size of the best use.
+    const uint32_t G_ = S / 16, H_ = num_q_heads + a.Hk;
+    uint64_t tpb = tpb_max;
+    double best = -1.0;
+    for (uint64_t c = tpb_max; c >= 1; --c) {
+        uint64_t sl = kConsumers / (c * G_);
+        if (sl < 1) sl = 1;
+        if (sl > H_) sl = H_;
+        const uint64_t units = c * G_ * sl;
+        const uint64_t passes = (units + kConsumers - 1) / kConsumers;
+        const uint64_t hps = (H_ + sl - 1) / sl;
+        const double use = (double)units / (double)(passes * kConsumers) *
+                           ((double)H_ / (double)sl) / (double)hps;
+        if (use >= 0.85) {
+            tpb = c;
+            break;
+        }
+        if (use > best + 1e-9) {
+            best = use;
+            tpb = c;
+        }
+    }
     a.tpb = (uint32_t)tpb;
     a.groups = (uint32_t)((tot_seq_len + tpb - 1) / tpb);
     a.tables_bytes = tables;
