@@ -361,67 +361,52 @@ cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
 
 // ------------------------------------------------------------------------
 // Register-staged variant, used for mrope.  With three position rows per
-// token the pipelined kernel would need three small freqs copies per token,
-// and tiny bulk copies cost more than they save; here the CTA has one thread
-// per 8-pair item of a token (rounded up to warps) and walks TPB tokens:
-// query loads first, then the ragged lookup, then every thread helps gather
-// the tokens' composed (cos, sin) rows into shared memory (one round trip),
-// then key rows are loaded and everything is rotated and stored.
-template <bool INTERLEAVED, int TPB, bool FP8K>
-__global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
-    extern __shared__ uint32_t s_dyn[];
-    uint32_t* s_off = s_dyn;
-    uint32_t* s_clen = s_dyn + a.B + 1;
-    __shared__ __align__(16) float s_cs[TPB][kMaxHead];  // composed (cos, sin) per pair
-    __shared__ int64_t s_kbase[TPB];
-    __shared__ int s_bad[TPB];
+// token the pipelined kernel would need three small freqs copies per token
+// (or a composed row built by the producer warp), and both measured slower
+// than this.  The CTA has one thread per 8-pair item of a token (rounded up
+// to warps) and is persistent: it stages the ragged tables once, then walks
+// groups of TPB tokens.  For the group in hand, every thread loads its query
+// vectors and (slot rows already known) its key vectors; while those loads
+// are in flight it prepares the next group into the other half of a
+// double-buffered shared area -- slot rows and position checks (one thread
+// per token) and the composed (cos, sin) row of each token (all threads,
+// one pair each) -- then rotates and stores the group in hand.
+template <int TPB>
+struct StagedSmem {
+    float cs[2][TPB][kMaxHead];  // composed (cos, sin) per pair
+    int64_t kbase[2][TPB];       // slot row of each token (-1: no page)
+    int bad[2][TPB];             // a RoPE position of the token is out of range
+};
 
-    const uint32_t groups = a.S >> 4;  // items per head
+template <int TPB>
+__device__ __forceinline__ void staged_prepare(const GqaArgs& a, const uint32_t* s_off,
+                                               const uint32_t* s_clen, StagedSmem<TPB>& sm,
+                                               uint32_t buf, uint32_t group) {
+    const uint32_t t_begin = group * TPB;
     const uint32_t i = threadIdx.x;
-    const bool has_item = i < a.items;
-    const uint32_t h = has_item ? i / groups : 0u;
-    const uint32_t m = has_item ? i % groups : 0u;
-    const bool is_q = has_item && h < a.Hq;
-    const uint32_t t_begin = blockIdx.x * TPB;
-    // element offsets of the two vectors of this item inside a head row
-    const uint32_t e0 = INTERLEAVED ? 16u * m : 8u * m;
-    const uint32_t e1 = INTERLEAVED ? 16u * m + 8u : (a.S >> 1) + 8u * m;
-
-    if (i < TPB) s_bad[i] = 0;
-
-    // phase 0: query data
-    uint4 xa[TPB], xb[TPB];
-#pragma unroll
-    for (int u = 0; u < TPB; ++u) {
-        xa[u] = make_uint4(0, 0, 0, 0);
-        xb[u] = xa[u];
-        const uint32_t t = t_begin + u;
-        if (is_q && t < a.T) {
-            const uint16_t* row = a.q_in + ((uint64_t)t * a.Hq + h) * a.S;
-            xa[u] = ld_stream(reinterpret_cast<const uint4*>(row + e0));
-            xb[u] = ld_stream(reinterpret_cast<const uint4*>(row + e1));
-        }
-    }
-
-    // phase 1: ragged metadata (contains a __syncthreads, so s_bad is ready)
-    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
-        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
-        return;
-    }
-
-    // phase 2a: slot row of each token
     if (i < TPB) {
         const uint32_t t = t_begin + i;
         int64_t base = -1;
+        int bad = 0;
         if (t < a.T) {
             const uint32_t b = find_request(s_off, a.B, t);
             const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
             base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
                             a.s_token, a.layer_off, b, pos);
+            if (a.mode == 0) {
+                bad = pos >= a.freqs_rows;
+            } else if (a.mode == 1) {
+                bad = __ldg(a.position_ids + t) >= a.freqs_rows;
+            } else {
+                for (uint32_t r = 0; r < 3; ++r)
+                    if (a.span_hi[r] > a.span_lo[r] &&
+                        __ldg(a.position_ids + (uint64_t)r * a.T + t) >= a.freqs_rows)
+                        bad = 1;
+            }
         }
-        s_kbase[i] = base;
+        sm.kbase[buf][i] = base;
+        sm.bad[buf][i] = bad;
     }
-    // phase 2b: composed freqs rows, one (cos, sin) pair per rotary pair
     const uint32_t half = a.S >> 1;
     for (uint32_t idx = threadIdx.x; idx < TPB * half; idx += blockDim.x) {
         const uint32_t u = idx / half, k = idx % half;
@@ -437,21 +422,55 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
             p = __ldg(a.position_ids + (uint64_t)section_of(a, k) * a.T + t);
         }
         float2 cs = make_float2(0.f, 0.f);
-        if (p < a.freqs_rows)
-            cs = __ldg(reinterpret_cast<const float2*>(a.freqs + p * a.S) + k);
-        else
-            s_bad[u] = 1;
-        *reinterpret_cast<float2*>(&s_cs[u][2 * k]) = cs;
+        if (p < a.freqs_rows) cs = __ldg(reinterpret_cast<const float2*>(a.freqs + p * a.S) + k);
+        *reinterpret_cast<float2*>(&sm.cs[buf][u][2 * k]) = cs;
     }
+}
+
+template <bool INTERLEAVED, int TPB, bool FP8K>
+__global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t* s_off = s_dyn;
+    uint32_t* s_clen = s_dyn + a.B + 1;
+    __shared__ __align__(16) StagedSmem<TPB> sm;
+
+    const uint32_t groups = a.S >> 4;  // items per head
+    const uint32_t i = threadIdx.x;
+    const bool has_item = i < a.items;
+    const uint32_t h = has_item ? i / groups : 0u;
+    const uint32_t m = has_item ? i % groups : 0u;
+    const bool is_q = has_item && h < a.Hq;
+    // element offsets of the two vectors of this item inside a head row
+    const uint32_t e0 = INTERLEAVED ? 16u * m : 8u * m;
+    const uint32_t e1 = INTERLEAVED ? 16u * m + 8u : (a.S >> 1) + 8u * m;
+
+    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    const uint32_t ngroups = (a.T + TPB - 1) / TPB;
+    uint32_t g = blockIdx.x;
+    if (g >= ngroups) return;
+    staged_prepare<TPB>(a, s_off, s_clen, sm, 0, g);
     __syncthreads();
 
-    // phase 3a: key data (needs the slot rows)
-    if (has_item && !is_q) {
+    for (uint32_t buf = 0; g < ngroups; g += gridDim.x, buf ^= 1u) {
+        const uint32_t t_begin = g * TPB;
+        // query and key data of the group in hand
+        uint4 xa[TPB], xb[TPB];
 #pragma unroll
         for (int u = 0; u < TPB; ++u) {
-            const int64_t kb = s_kbase[u];
-            if (kb >= 0 && !s_bad[u]) {
-                const unsigned char* row = a.cache + (kb + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
+            xa[u] = make_uint4(0, 0, 0, 0);
+            xb[u] = xa[u];
+            const uint32_t t = t_begin + u;
+            if (t >= a.T || sm.bad[buf][u]) continue;
+            if (is_q) {
+                const uint16_t* row = a.q_in + ((uint64_t)t * a.Hq + h) * a.S;
+                xa[u] = ld_stream(reinterpret_cast<const uint4*>(row + e0));
+                xb[u] = ld_stream(reinterpret_cast<const uint4*>(row + e1));
+            } else if (has_item && sm.kbase[buf][u] >= 0) {
+                const unsigned char* row =
+                    a.cache + (sm.kbase[buf][u] + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
                 if (FP8K) {  // 8 codes per vector: kept in .x/.y
                     const uint2 va8 = *reinterpret_cast<const uint2*>(row + e0);
                     const uint2 vb8 = *reinterpret_cast<const uint2*>(row + e1);
@@ -463,71 +482,83 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
                 }
             }
         }
-    }
-    if (i < TPB && t_begin + i < a.T) {
-        if (s_bad[i])
-            flag(a.err_flags, KVW_ERR_POSITION);
-        else if (s_kbase[i] < 0)
-            flag(a.err_flags, KVW_ERR_PAGE);
-    }
-    if (!has_item) return;
-
-    // phase 3b: rotate and store
+        // the next group, while those loads are in flight
+        if (g + gridDim.x < ngroups) staged_prepare<TPB>(a, s_off, s_clen, sm, buf ^ 1u, g + gridDim.x);
+        if (i < TPB && t_begin + i < a.T) {
+            if (sm.bad[buf][i])
+                flag(a.err_flags, KVW_ERR_POSITION);
+            else if (sm.kbase[buf][i] < 0)
+                flag(a.err_flags, KVW_ERR_PAGE);
+        }
+        if (has_item) {
 #pragma unroll
-    for (int u = 0; u < TPB; ++u) {
-        const uint32_t t = t_begin + u;
-        if (t >= a.T || s_bad[u]) continue;
-        if (!is_q && s_kbase[u] < 0) continue;
-        const float4* cs4 = reinterpret_cast<const float4*>(&s_cs[u][16u * m]);
-        const float4 c0 = cs4[0], c1 = cs4[1], c2 = cs4[2], c3 = cs4[3];
-        const float c[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
-        const float s[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
-        float va[8], vb[8], ya[8], yb[8];
-        if (FP8K && !is_q) {
-            unpack8_e4m3(make_uint2(xa[u].x, xa[u].y), va);
-            unpack8_e4m3(make_uint2(xb[u].x, xb[u].y), vb);
-            if (a.kscale != 1.0f) {
+            for (int u = 0; u < TPB; ++u) {
+                const uint32_t t = t_begin + u;
+                if (t >= a.T || sm.bad[buf][u]) continue;
+                if (!is_q && sm.kbase[buf][u] < 0) continue;
+                const float4* cs4 = reinterpret_cast<const float4*>(&sm.cs[buf][u][16u * m]);
+                const float4 c0 = cs4[0], c1 = cs4[1], c2 = cs4[2], c3 = cs4[3];
+                const float c[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
+                const float s[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
+                float va[8], vb[8], ya[8], yb[8];
+                if (FP8K && !is_q) {
+                    unpack8_e4m3(make_uint2(xa[u].x, xa[u].y), va);
+                    unpack8_e4m3(make_uint2(xb[u].x, xb[u].y), vb);
+                    if (a.kscale != 1.0f) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    va[q] = __fmul_rn(va[q], a.kscale);
-                    vb[q] = __fmul_rn(vb[q], a.kscale);
+                        for (int q = 0; q < 8; ++q) {
+                            va[q] = __fmul_rn(va[q], a.kscale);
+                            vb[q] = __fmul_rn(vb[q], a.kscale);
+                        }
+                    }
+                } else {
+                    unpack8(xa[u], va);
+                    unpack8(xb[u], vb);
+                }
+                if (INTERLEAVED) {  // pairs (va0,va1) (va2,va3) .. (vb6,vb7)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        rope_pair(va[2 * q], va[2 * q + 1], c[q], s[q], ya[2 * q], ya[2 * q + 1]);
+                        rope_pair(vb[2 * q], vb[2 * q + 1], c[q + 4], s[q + 4], yb[2 * q],
+                                  yb[2 * q + 1]);
+                    }
+                } else {  // pairs (va[q], vb[q])
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) rope_pair(va[q], vb[q], c[q], s[q], ya[q], yb[q]);
+                }
+                if (is_q) {
+                    uint16_t* row = a.q_out + ((uint64_t)t * a.Hq + h) * a.S;
+                    st_stream(reinterpret_cast<uint4*>(row + e0), pack8_bf16(ya));
+                    st_stream(reinterpret_cast<uint4*>(row + e1), pack8_bf16(yb));
+                } else {
+                    unsigned char* row =
+                        a.cache + (sm.kbase[buf][u] + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
+                    store_k8<FP8K>(row + e0 * a.kesz, ya, a.kscale);
+                    store_k8<FP8K>(row + e1 * a.kesz, yb, a.kscale);
                 }
             }
-        } else {
-            unpack8(xa[u], va);
-            unpack8(xb[u], vb);
         }
-        if (INTERLEAVED) {  // pairs (va0,va1) (va2,va3) .. (vb6,vb7)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                rope_pair(va[2 * q], va[2 * q + 1], c[q], s[q], ya[2 * q], ya[2 * q + 1]);
-                rope_pair(vb[2 * q], vb[2 * q + 1], c[q + 4], s[q + 4], yb[2 * q], yb[2 * q + 1]);
-            }
-        } else {  // pairs (va[q], vb[q])
-#pragma unroll
-            for (int q = 0; q < 8; ++q) rope_pair(va[q], vb[q], c[q], s[q], ya[q], yb[q]);
-        }
-        if (is_q) {
-            uint16_t* row = a.q_out + ((uint64_t)t * a.Hq + h) * a.S;
-            st_stream(reinterpret_cast<uint4*>(row + e0), pack8_bf16(ya));
-            st_stream(reinterpret_cast<uint4*>(row + e1), pack8_bf16(yb));
-        } else {
-            unsigned char* row = a.cache + (s_kbase[u] + (int64_t)(h - a.Hq) * a.s_head) * a.kesz;
-            store_k8<FP8K>(row + e0 * a.kesz, ya, a.kscale);
-            store_k8<FP8K>(row + e1 * a.kesz, yb, a.kscale);
-        }
+        __syncthreads();  // next group's tables visible; this group's no longer read
     }
 }
 
 template <bool INTERLEAVED, int TPB, bool FP8K>
 cudaError_t launch_staged(const GqaArgs& a, uint32_t threads, size_t smem, cudaStream_t stream) {
     auto k = qk_rope_staged_kernel<INTERLEAVED, TPB, FP8K>;
+    cudaError_t e;
     if (smem > 16 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const uint32_t blocks = (a.T + TPB - 1) / TPB;
-    k<<<blocks, threads, smem, stream>>>(a);
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, smem)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const uint64_t groups = (a.T + TPB - 1) / TPB;
+    const uint64_t wave = (uint64_t)sms * per_sm;
+    k<<<(uint32_t)(groups < wave ? groups : wave), threads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
