@@ -195,7 +195,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, name, budget_s):
+def cpu_baseline(w, name, budget_s, single_thread=True):
     """The oracle, as it is, on the host cores, over whole batches of the
     same workload until ``budget_s`` seconds of CPU time have elapsed."""
     import oracle
@@ -230,18 +230,36 @@ def cpu_baseline(w, name, budget_s):
         fn = ((lambda: oracle.quantize_rows_e4m3(w.x)) if w.per_row
               else (lambda: oracle.convert_bf16_to_e4m3(w.x, w.scale)))
     fn()  # warm: page in buffers
-    n, t0 = 0, time.perf_counter()
-    while True:
-        fn()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
+
+    def timed(f, budget):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            f()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return n, el
+
+    n, el = timed(fn, budget_s)
     tps = n * w.T / el
-    return {"value": tps, "unit": "tokens/s" if k not in ("gather", "codec") else "rows/s",
-            "cores": threads, "kind": "oracle",
-            "sample": "%d whole batches of %d units (%s), %.1f s wall" % (n, w.T, name, el),
-            "gbs": algorithmic_bytes(w, name) * n / el / 1e9}
+    res = {"value": tps, "unit": "tokens/s" if k not in ("gather", "codec") else "rows/s",
+           "cores": threads, "kind": "oracle",
+           "sample": "%d whole batches of %d units (%s), %.1f s wall" % (n, w.T, name, el),
+           "gbs": algorithmic_bytes(w, name) * n / el / 1e9}
+    if single_thread and threads > 1 and k in ("mla", "gqa", "kno"):
+        # the same oracle on one thread, over a shorter bounded sample
+        kw = {"out_dtype": w.q_out_dtype} if k == "mla" else {}
+        one = {"mla": lambda: (oracle.mla_rope_rmsnorm_inplace if w.inplace
+                               else oracle.mla_rope_rmsnorm_quant)(w, q_rope_out=q_out,
+                                                                   cache_data=cache, nthreads=1,
+                                                                   **kw),
+               "gqa": lambda: oracle.qk_rope_paged_ragged(w, output=out, cache_data=cache,
+                                                          nthreads=1),
+               "kno": lambda: oracle.rms_norm_kv_cache_paged(w, cache_data=cache, nthreads=1)}[k]
+        n1, el1 = timed(one, budget_s / 3)
+        res["single_thread"] = {"value": n1 * w.T / el1, "cores": 1,
+                                "sample": "%d whole batches, %.1f s wall" % (n1, el1)}
+    return res
 
 
 def run_reference(args):
@@ -258,7 +276,7 @@ def run_reference(args):
     # keep the whole run within about two minutes whatever K and W are
     step_s = min(args.ref_step_s, 120.0 / (args.warmup + args.steps))
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, name, budget_s=step_s)
+        cb = cpu_baseline(w, name, budget_s=step_s, single_thread=False)
         threads = cb["cores"]
         if i >= args.warmup:
             times.append(w.T / cb["value"])
