@@ -378,9 +378,11 @@ def run_ours(args):
         e2e = {"value": tokens_all / (e2e["ms"] / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                "ms_per_step": e2e["ms"],
-               "how": "pinned host inputs -> device, kvw call, results -> pinned host, every "
-                      "step; steps pipelined %d deep on copy-in / compute / copy-out streams, "
-                      "8 steps per CUDA graph replay" % e2e["depth"]}
+               "how": "every step: one copy of its packed inputs (and a zeroed error word) "
+                      "from pinned host memory, the kvw call, one copy of the error word and "
+                      "the outputs back to pinned host memory; steps pipelined %d deep on "
+                      "copy-in / compute / copy-out streams, %d steps per CUDA graph replay" % (
+                          e2e["depth"], e2e["per_graph"])}
 
     peak, peak_src = measured_peak()
     achieved = abytes / (ms / 1000.0) / 1e9
@@ -419,104 +421,137 @@ def run_ours(args):
     return 0
 
 
-def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=2):
+def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=3, per_graph=32, chunks=1):
     """Throughput through the public API with host buffers: every step copies
     its inputs from pinned host memory, launches the entry point and copies
-    its results back.  Steps are pipelined ``depth`` deep over separate
+    its results back.  Each step's I/O lives in one device buffer laid out as
+    [inputs | error word | outputs] (16-byte aligned pieces), mirrored by
+    pinned host buffers, so a step is one host->device copy of the inputs and
+    a zeroed error word, the kvw call, and one device->host copy of the error
+    word and the outputs.  Steps are pipelined ``depth`` deep over separate
     copy-in, compute and copy-out streams (a serving loop overlaps step i's
     compute with step i+1's inputs and step i-1's results), each buffer set
-    reused only after the step that last used it is done."""
+    reused only after the step that last used it is done; ``per_graph`` steps
+    are captured in one CUDA graph.  Each copy is split into ``chunks`` pieces
+    on as many streams, so that several copy engines share it."""
     import ctypes
 
     import torch
 
     from gqa_kv_cache_mla_gb300 import kvw
 
-    def pinned(t):
-        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+    if k == "mla":
+        ins = [("q", d.q.tensor), ("kv", d.kv.tensor), ("off", d.offsets.tensor),
+               ("clen", d.cache_lengths.tensor), ("pt", d.page_table.tensor)]
+        outs = [("q_out", d.q_out.tensor)]
+    elif k == "gqa":
+        ins = [("q", d.q.tensor), ("off", d.offsets.tensor), ("clen", d.cache_lengths.tensor),
+               ("pt", d.page_table.tensor)]
+        if d.pos is not None:
+            ins.append(("pos", d.pos.tensor))
+        outs = [("out", d.out.tensor)]
+    else:
+        ins = [("off", d.offsets.tensor), ("clen", d.cache_lengths.tensor),
+               ("pt", d.page_table.tensor)]
+        outs = []
+
+    def up16(x):
+        return (x + 15) // 16 * 16
+
+    layout, pos = {}, 0
+    for name, t in ins:
+        layout[name] = (pos, t)
+        pos = up16(pos + t.numel() * t.element_size())
+    err_at = pos
+    pos += 16
+    for name, t in outs:
+        layout[name] = (pos, t)
+        pos = up16(pos + t.numel() * t.element_size())
+    total = pos
+    h2d, d2h = err_at + 16, total - err_at  # [inputs | err] in, [err | outputs] out
+
+    def view(buf, name):
+        o, t = layout[name]
+        n = t.numel() * t.element_size()
+        return buf[o:o + n].view(t.dtype).view(t.shape)
 
     sets = []
-    for i in range(depth):
-        if k == "mla":
-            ins = {"q": d.q.tensor, "kv": d.kv.tensor, "off": d.offsets.tensor,
-                   "clen": d.cache_lengths.tensor, "pt": d.page_table.tensor}
-            outs = {"q_out": d.q_out.tensor, "err": d.err.tensor}
-        elif k == "gqa":
-            ins = {"q": d.q.tensor, "off": d.offsets.tensor, "clen": d.cache_lengths.tensor,
-                   "pt": d.page_table.tensor}
-            if d.pos is not None:
-                ins["pos"] = d.pos.tensor
-            outs = {"out": d.out.tensor, "err": d.err.tensor}
-        else:
-            ins = {"off": d.offsets.tensor, "clen": d.cache_lengths.tensor,
-                   "pt": d.page_table.tensor}
-            outs = {"err": d.err.tensor}
-        h_in = {n: pinned(t) for n, t in ins.items()}  # the step's inputs, on the host
-        if i > 0:  # its own device buffers
-            ins = {n: torch.empty_like(t) for n, t in ins.items()}
-            outs = {n: torch.empty_like(t) for n, t in outs.items()}
+    for _ in range(depth):
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+        h_in = torch.zeros(h2d, dtype=torch.uint8, pin_memory=True)  # error word stays 0
+        for name, t in ins:
+            o, _ = layout[name]
+            n = t.numel() * t.element_size()
+            h_in[o:o + n].copy_(t.reshape(-1).view(torch.uint8).cpu())
+        h_out = torch.empty(d2h, dtype=torch.uint8, pin_memory=True)
+        v = {name: view(dbuf, name) for name in layout}
+        v["err"] = dbuf[err_at:err_at + 4].view(torch.int32)
         desc = kvw.PagedCacheT()
         ctypes.memmove(ctypes.byref(desc), ctypes.byref(d.desc), ctypes.sizeof(desc))
-        desc.page_table = ins["pt"].data_ptr()
-        desc.cache_lengths = ins["clen"].data_ptr()
-        h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
-        sets.append(dict(ins=ins, outs=outs, desc=desc, h_in=h_in, h_out=h_out,
-                         computed=torch.cuda.Event(), copied_out=torch.cuda.Event()))
-    h2d = sum(t.numel() * t.element_size() for t in sets[0]["h_in"].values())
-    d2h = sum(t.numel() * t.element_size() for t in sets[0]["h_out"].values())
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        desc.page_table = v["pt"].data_ptr()
+        desc.cache_lengths = v["clen"].data_ptr()
+        sets.append(dict(dbuf=dbuf, v=v, desc=desc, h_in=h_in, h_out=h_out,
+                         computed=torch.cuda.Event(), copied_out=[]))
+    s_ins = [torch.cuda.Stream(dev) for _ in range(chunks)]
+    s_outs = [torch.cuda.Stream(dev) for _ in range(chunks)]
+
+    def pieces(n):  # [lo, hi) byte ranges, 16-byte aligned
+        step_ = up16((n + chunks - 1) // chunks)
+        return [(lo, min(n, lo + step_)) for lo in range(0, n, step_)]
 
     def call(S, stream):
-        i, o = S["ins"], S["outs"]
+        v = S["v"]
         if k == "mla":
-            kvw.kvw_mla_rope_rmsnorm_quant(o["q_out"], i["q"], i["off"], d.freqs.tensor,
-                                           d.gamma.tensor, i["kv"], S["desc"], w.layer_idx,
-                                           w.epsilon, o["err"], stream,
+            kvw.kvw_mla_rope_rmsnorm_quant(v["q_out"], v["q"], v["off"], d.freqs.tensor,
+                                           d.gamma.tensor, v["kv"], S["desc"], w.layer_idx,
+                                           w.epsilon, v["err"], stream,
                                            kv_row_stride=w.kv_in.shape[-1])
         elif k == "gqa":
             kvw.kvw_qk_rope_paged_ragged(
-                i["q"], i["off"], S["desc"], d.freqs.tensor, i.get("pos"), w.interleaved,
-                None if w.mrope_section is None else [int(v) for v in w.mrope_section],
-                w.layer_idx, o["out"], o["err"], stream)
+                v["q"], v["off"], S["desc"], d.freqs.tensor, v.get("pos"), w.interleaved,
+                None if w.mrope_section is None else [int(x) for x in w.mrope_section],
+                w.layer_idx, v["out"], v["err"], stream)
         else:
             kvw.kvw_rms_norm_kv_cache_paged(S["desc"], d.gamma.tensor, w.epsilon,
-                                            w.weight_offset, w.layer_idx, w.T, i["off"],
-                                            w.multiply_before_cast, w.per_head_norm, o["err"],
+                                            w.weight_offset, w.layer_idx, w.T, v["off"],
+                                            w.multiply_before_cast, w.per_head_norm, v["err"],
                                             stream)
 
-    def step(n, S, comp, first):
-        in_ready = torch.cuda.Event()
-        s_in.wait_stream(comp) if first else s_in.wait_event(S["computed"])
-        with torch.cuda.stream(s_in):
-            for name, t in S["ins"].items():
-                t.copy_(S["h_in"][name], non_blocking=True)
-            in_ready.record(s_in)
-        comp.wait_event(in_ready)
-        if not first:
-            comp.wait_event(S["copied_out"])  # its outputs were read back
+    def step(S, comp, first):
+        for j, (lo, hi) in enumerate(pieces(h2d)):
+            s_in = s_ins[j]
+            s_in.wait_stream(comp) if first else s_in.wait_event(S["computed"])
+            if not first:
+                for e in S["copied_out"]:
+                    s_in.wait_event(e)  # its previous results were read back
+            in_ready = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                S["dbuf"][lo:hi].copy_(S["h_in"][lo:hi], non_blocking=True)
+                in_ready.record(s_in)
+            comp.wait_event(in_ready)
         with torch.cuda.stream(comp):
-            S["outs"]["err"].zero_()
             call(S, comp)
             S["computed"].record(comp)
-        s_out.wait_event(S["computed"])
-        with torch.cuda.stream(s_out):
-            for name, t in S["outs"].items():
-                S["h_out"][name].copy_(t, non_blocking=True)
-            S["copied_out"].record(s_out)
+        S["copied_out"] = []
+        for j, (lo, hi) in enumerate(pieces(d2h)):
+            s_out = s_outs[j]
+            s_out.wait_event(S["computed"])
+            with torch.cuda.stream(s_out):
+                S["h_out"][lo:hi].copy_(S["dbuf"][err_at + lo:err_at + hi], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_out)
+                S["copied_out"].append(e)
 
-    # K steps per CUDA graph: the copy-in / compute / copy-out streams overlap
-    # inside the graph and one graph launch replaces ~13 host calls per step
-    K = 4 * depth
+    K = max(depth, per_graph // depth * depth)
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(dev)
     with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
         for n in range(K):
-            step(n, sets[n % depth], cap, first=n < depth)
-        s_in_done, s_out_done = torch.cuda.Event(), torch.cuda.Event()
-        s_in_done.record(s_in)
-        s_out_done.record(s_out)
-        cap.wait_event(s_in_done)
-        cap.wait_event(s_out_done)
+            step(sets[n % depth], cap, first=n < depth)
+        for st in s_ins + s_outs:  # join every side stream back into the capture
+            done = torch.cuda.Event()
+            done.record(st)
+            cap.wait_event(done)
     reps = max(1, (steps + K - 1) // K)
     for _ in range(max(1, warmup // K)):
         graph.replay()
@@ -529,9 +564,16 @@ def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=2):
     b.record(launch)
     torch.cuda.synchronize()
     for S in sets:
-        assert int(S["h_out"]["err"][0]) == 0, "data errors in the e2e run"
+        assert int(S["h_out"][:4].view(torch.int32)[0]) == 0, "data errors in the e2e run"
+    if outs:  # the results read back equal the device path's results
+        name, t = outs[0]
+        o = layout[name][0] - err_at
+        n = t.numel() * t.element_size()
+        assert torch.equal(sets[0]["h_out"][o:o + n], t.reshape(-1).view(torch.uint8).cpu()), \
+            "e2e results differ from the device run"
     steps = reps * K
-    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h, "depth": depth}
+    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h, "depth": depth,
+            "per_graph": K, "chunks": chunks}
 
 
 def main():
