@@ -505,7 +505,8 @@ def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=3, per_graph=32, chun
             kvw.kvw_mla_rope_rmsnorm_quant(v["q_out"], v["q"], v["off"], d.freqs.tensor,
                                            d.gamma.tensor, v["kv"], S["desc"], w.layer_idx,
                                            w.epsilon, v["err"], stream,
-                                           kv_row_stride=w.kv_in.shape[-1])
+                                           kv_row_stride=w.kv_in.shape[-1],
+                                           out_dtype=w.q_out_dtype)
         elif k == "gqa":
             kvw.kvw_qk_rope_paged_ragged(
                 v["q"], v["off"], S["desc"], d.freqs.tensor, v.get("pos"), w.interleaved,

@@ -146,12 +146,30 @@ def paged_cache(data, dtype, page_table, cache_lengths, num_pages, num_layers, p
     return s
 
 
+def _out_dtype(out, out_dtype, name):
+    """The element type code of an output buffer: taken from the tensor's
+    element size when not given (1 byte: FP8 E4M3, 2 bytes: bf16), and
+    checked against it when given, so the kernel never writes a wider type
+    into a narrower buffer."""
+    size = out.element_size() if hasattr(out, "element_size") else None
+    if out_dtype is None:
+        if size not in (1, 2):
+            raise ValueError("%s: give out_dtype for an output without an element size" % name)
+        return DTYPE_FP8_E4M3 if size == 1 else DTYPE_BF16
+    want = {DTYPE_FP8_E4M3: 1, DTYPE_BF16: 2}.get(out_dtype)
+    if size is not None and want is not None and size != want:
+        raise ValueError("%s: out_dtype %d needs %d-byte elements, the output has %d" % (
+            name, out_dtype, want, size))
+    return out_dtype
+
+
 def kvw_mla_rope_rmsnorm_quant(q_rope_out, q_rope, input_row_offsets, freqs_cis, gamma, kv_in,
                                cache: PagedCacheT, layer_idx: int, epsilon: float, err_flags=None,
                                stream=None, *, num_batches=None, tot_seq_len=None,
                                num_heads=None, freqs_rows=None, kv_row_stride=None,
-                               out_dtype=DTYPE_BF16, freq_dtype=DTYPE_F32,
+                               out_dtype=None, freq_dtype=DTYPE_F32,
                                gamma_dtype=DTYPE_BF16, check=True) -> int:
+    out_dtype = _out_dtype(q_rope_out, out_dtype, "kvw_mla_rope_rmsnorm_quant")
     B = input_row_offsets.shape[0] - 1 if num_batches is None else num_batches
     T = q_rope.shape[0] if tot_seq_len is None else tot_seq_len
     H = q_rope.shape[1] if num_heads is None else num_heads
@@ -168,8 +186,9 @@ def kvw_mla_rope_rmsnorm_inplace(q_rope_out, q_rope, input_row_offsets, freqs_ci
                                  cache: PagedCacheT, layer_idx: int, epsilon: float,
                                  err_flags=None, stream=None, *, num_batches=None,
                                  tot_seq_len=None, num_heads=None, freqs_rows=None,
-                                 out_dtype=DTYPE_BF16, freq_dtype=DTYPE_F32,
+                                 out_dtype=None, freq_dtype=DTYPE_F32,
                                  gamma_dtype=DTYPE_BF16, check=True) -> int:
+    out_dtype = _out_dtype(q_rope_out, out_dtype, "kvw_mla_rope_rmsnorm_inplace")
     B = input_row_offsets.shape[0] - 1 if num_batches is None else num_batches
     T = q_rope.shape[0] if tot_seq_len is None else tot_seq_len
     H = q_rope.shape[1] if num_heads is None else num_heads
@@ -184,6 +203,7 @@ def kvw_mla_rope_rmsnorm_inplace(q_rope_out, q_rope, input_row_offsets, freqs_ci
 def kvw_mla_gather_latent(out, out_dtype: int, out_scale: float, cache: PagedCacheT,
                           layer_idx: int, ctx_offsets, err_flags=None, stream=None, *,
                           num_batches=None, total_rows=None, check=True) -> int:
+    out_dtype = _out_dtype(out, out_dtype, "kvw_mla_gather_latent")
     B = ctx_offsets.shape[0] - 1 if num_batches is None else num_batches
     rows = out.shape[0] if total_rows is None else total_rows
     st = lib.kvw_mla_gather_latent(_ptr(out), out_dtype, out_scale, ctypes.byref(cache),

@@ -191,3 +191,19 @@ def test_codec_host_checks():
     assert q(FAKE, FAKE, FAKE, 4, 60, 64, 64, 0) == kvw.KVW_EINVAL
     assert q(FAKE, FAKE, FAKE, 4, 64, 60, 64, 0) == kvw.KVW_EINVAL
     assert q(FAKE, FAKE, ODD, 4, 64, 64, 64, 0) == kvw.KVW_EINVAL
+
+
+def test_binding_output_type_follows_the_buffer():
+    """The binding derives the q / gather output type from the output tensor and
+    rejects a type wider than the buffer (the kernel would write past it)."""
+    import torch
+
+    u8 = torch.zeros(16, dtype=torch.uint8)
+    i16 = torch.zeros(16, dtype=torch.int16)
+    assert kvw._out_dtype(u8, None, "x") == kvw.DTYPE_FP8_E4M3
+    assert kvw._out_dtype(i16, None, "x") == kvw.DTYPE_BF16
+    assert kvw._out_dtype(i16, kvw.DTYPE_BF16, "x") == kvw.DTYPE_BF16
+    with pytest.raises(ValueError):
+        kvw._out_dtype(u8, kvw.DTYPE_BF16, "x")
+    with pytest.raises(ValueError):
+        kvw._out_dtype(i16, kvw.DTYPE_FP8_E4M3, "x")
