@@ -13,13 +13,13 @@
 // the team finishes the reduction, so no shared memory or block barrier is
 // needed for the norm itself.  Each team handles RPT rows so every thread has
 // RPT x VPL 16-byte loads in flight.  CTAs are persistent (one wave at the
-// occupancy the register count allows): a CTA stages the ragged tables once,
-// then walks tiles of rows_per_block rows.  The page slots of the few tokens
-// of the next tile are resolved (ragged lookup in shared memory, page table)
-// while the current tile's loads are in flight, into the other half of a
-// double-buffered shared array; then the tile is normalised and written back
-// in place.  Columns at or past gamma_len are neither read into the sum nor
-// written.
+// occupancy the register count allows) and stage the ragged tables and the
+// weights once; after that each warp walks its own tiles of teams x RPT rows
+// with no block barrier: it resolves the page slots of the few tokens of its
+// next tile (ragged lookup in shared memory, page table) into its slice of
+// shared memory while the current tile's loads are in flight, then
+// normalises the tile and writes it back in place.  Columns at or past
+// gamma_len are neither read into the sum nor written.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -29,7 +29,7 @@ namespace {
 
 constexpr uint32_t kThreads = 256;
 constexpr uint32_t kMaxCols = 2048;
-constexpr uint32_t kMaxTileTokens = kThreads * 2 + 2;  // tokens of up to 512 rows
+constexpr uint32_t kMaxWarpTileTokens = 66;  // tokens of a warp tile: up to 64 rows + 2
 
 struct KnArgs {
     uint16_t* cache;
@@ -44,7 +44,6 @@ struct KnArgs {
     uint32_t per_head;
     uint32_t tl_log2;         // team size = 1 << tl_log2
     uint32_t nv;              // 16-byte vectors per row = ceil(G / 8)
-    uint32_t rows_per_block;
     uint32_t rows;            // T * rows_per_token
     float eps, wo;
     int mbc;
@@ -58,12 +57,13 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
     uint32_t* s_clen = s_dyn + a.B + 1;
-    __shared__ int64_t s_base[2][kMaxTileTokens];
+    __shared__ int64_t s_wbase[kThreads / 32][kMaxWarpTileTokens];
 
     const uint32_t TL = 1u << a.tl_log2;
-    const uint32_t team = threadIdx.x >> a.tl_log2;
-    const uint32_t tl = threadIdx.x & (TL - 1u);
-    const uint32_t teams = kThreads >> a.tl_log2;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t team = lane >> a.tl_log2;   // team inside the warp
+    const uint32_t tl = lane & (TL - 1u);
+    const uint32_t teams = 32u >> a.tl_log2;   // teams per warp
 
     // weights gamma + weight_offset of the normalised columns, in shared memory
     // (zero past gamma_len), read as float4 pairs by the lanes of each column
@@ -76,31 +76,37 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
         if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
         return;
     }
-    const uint32_t tiles = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
-    uint32_t tile = blockIdx.x;
-    if (tile >= tiles) return;
-    // page slot of every token of a tile -> dst[token - first token of the tile]
-    auto resolve = [&](uint32_t tl_idx, int64_t* dst) {
-        const uint32_t r0 = tl_idx * a.rows_per_block;
+    // Warp tiles of teams x RPT consecutive rows, walked by each warp on its
+    // own (no block barrier after the set-up above).  The page slot of every
+    // token of a tile sits in the warp's slice of shared memory: the warp
+    // resolves the next tile's slots after reading the current ones and
+    // while the current tile's loads are in flight.
+    const uint32_t rows_wt = teams * RPT;
+    const uint32_t wtiles = (a.rows + rows_wt - 1) / rows_wt;
+    const uint32_t nwarps = gridDim.x * (kThreads / 32);
+    int64_t* wbase = s_wbase[warp];
+    auto resolve = [&](uint32_t wt) {
+        const uint32_t r0 = wt * rows_wt;
         const uint32_t t_lo = r0 / a.rows_per_token;
-        const uint32_t t_hi = (min(r0 + a.rows_per_block, a.rows) - 1) / a.rows_per_token;
-        for (uint32_t k = threadIdx.x; k <= t_hi - t_lo; k += kThreads) {
+        const uint32_t t_hi = (min(r0 + rows_wt, a.rows) - 1) / a.rows_per_token;
+        for (uint32_t k = lane; k <= t_hi - t_lo; k += 32) {
             const uint32_t t = t_lo + k;
             const uint32_t b = find_request(s_off, a.B, t);
             const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
             const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size,
                                           a.s_page, a.s_token, a.layer_off, b, pos);
-            dst[k] = base;
+            wbase[k] = base;
             if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
         }
     };
-    resolve(tile, s_base[0]);
-    __syncthreads();
+    uint32_t wt = blockIdx.x * (kThreads / 32) + warp;
+    if (wt < wtiles) resolve(wt);
+    __syncwarp();
 
-    for (uint32_t buf = 0; tile < tiles; tile += gridDim.x, buf ^= 1u) {
-    const uint32_t r0 = tile * a.rows_per_block;
+    for (; wt < wtiles; wt += nwarps) {
+    const uint32_t r0 = wt * rows_wt;
     const uint32_t t_lo = r0 / a.rows_per_token;
-    const uint32_t r_end = min(r0 + a.rows_per_block, a.rows);
+    const uint32_t r_end = min(r0 + rows_wt, a.rows);
 
     // pointers of this lane's first vector in each of its rows (null: no row);
     // row r = r0 + team + q * teams, walked as (token, head) without dividing
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
         const uint32_t r = r0 + team + q * teams;
         ptr[q] = nullptr;
         if (r < r_end) {
-            const int64_t base = s_base[buf][t - t_lo];
+            const int64_t base = wbase[t - t_lo];
             if (base >= 0) ptr[q] = a.cache + base + (a.per_head ? (int64_t)g * a.s_head : 0);
         }
         t += dt;
@@ -133,7 +139,9 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
             }
         }
     }
-    if (tile + gridDim.x < tiles) resolve(tile + gridDim.x, s_base[buf ^ 1u]);
+    __syncwarp();  // every lane has read this tile's slots
+    if (wt + nwarps < wtiles) resolve(wt + nwarps);
+    __syncwarp();  // the next tile's slots are visible to the whole warp
 
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
@@ -178,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
             }
         }
     }
-    __syncthreads();  // next tile's slots visible; this tile's no longer read
     }
 }
 
@@ -189,7 +196,9 @@ cudaError_t launch_one(const KnArgs& a, size_t smem, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const uint32_t tiles = (a.rows + a.rows_per_block - 1) / a.rows_per_block;
+    const uint32_t rows_wt = (32u >> a.tl_log2) * RPT;
+    const uint32_t wtiles = (a.rows + rows_wt - 1) / rows_wt;
+    const uint32_t tiles = (wtiles + kThreads / 32 - 1) / (kThreads / 32);  // CTAs with work
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -280,20 +289,14 @@ extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const
     a.wo = weight_offset;
     a.mbc = multiply_before_cast ? 1 : 0;
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
-    const uint32_t teams = kThreads / tl;
     cudaError_t e;
-    if (vpl <= 1) {
-        a.rows_per_block = teams * 8;
+    if (vpl <= 1)
         e = launch<1, 8>(a, smem, stream);
-    } else if (vpl <= 2) {
-        a.rows_per_block = teams * 4;
+    else if (vpl <= 2)
         e = launch<2, 4>(a, smem, stream);
-    } else if (vpl <= 4) {
-        a.rows_per_block = teams * 2;
+    else if (vpl <= 4)
         e = launch<4, 2>(a, smem, stream);
-    } else {
-        a.rows_per_block = teams;
+    else
         e = launch<8, 1>(a, smem, stream);
-    }
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }
