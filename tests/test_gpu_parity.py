@@ -395,6 +395,10 @@ def test_max_batches_all_entry_points(orc, dev):
     run_gqa(orc, dev, g)
     k = W.knorm_workload("mb", 904, new, prior, 2, 64, page_size=32, gamma_len=64)
     run_knorm(orc, dev, k)
+    w2 = W.mla_workload("mb", 905, new, prior, num_heads=2, page_size=32, max_seq_len=128,
+                        cache_dtype=W.DTYPE_BF16)
+    run_mla(orc, dev, W.mla_inplace(w2))
+    run_gather(orc, dev, W.mla_gather(w2, out_dtype=W.DTYPE_FP8_E4M3))
 
 
 @pytest.mark.parametrize("name", ["knorm128_cast_first", "knorm_whole_row"])
@@ -412,6 +416,13 @@ def test_mla_fp8_q_output(orc, dev, build):
 
     w = {"tiny": lambda: W.mla_tiny(W.DTYPE_FP8_E4M3), "decode": lambda: W.mla_decode(),
          "prefill": lambda: W.mla_prefill(W.DTYPE_FP8_E4M3)}[build]()
+    run_mla(orc, dev, dataclasses.replace(w, q_out_dtype=W.DTYPE_FP8_E4M3))
+
+
+def test_mla_inplace_fp8_q_output(orc, dev):
+    import dataclasses
+
+    w = W.mla_inplace(W.mla_decode(W.DTYPE_FP8_E4M3))
     run_mla(orc, dev, dataclasses.replace(w, q_out_dtype=W.DTYPE_FP8_E4M3))
 
 
@@ -592,6 +603,33 @@ def test_quantize_rows_every_scale_mantissa(orc, dev, shift):
     bad = np.flatnonzero(got != codes)
     assert bad.size == 0, (bad.size, x.reshape(-1)[bad[:5]], got.reshape(-1)[bad[:5]],
                            codes.reshape(-1)[bad[:5]])
+
+
+@pytest.mark.parametrize("rows,cols,in_stride,out_stride", [
+    (24, 4096, 4096, 4096),    # longer than 2048: the two-pass kernel
+    (33, 3000, 3008, 3000),    # ragged last vector group, padded input rows
+    (40, 576, 640, 600),       # register kernel with strided rows on both sides
+])
+def test_quantize_rows_long_and_strided(orc, dev, rows, cols, in_stride, out_stride):
+    import torch
+
+    from gqa_kv_cache_mla_gb300 import kvw
+
+    rng = np.random.default_rng(850 + cols)
+    x = W.normal_bf16(rng, (rows, in_stride), outlier_frac=0.02)
+    d = dev.Guarded(x, "cuda")
+    out0 = np.full((rows, out_stride), 0x5A, np.uint8)
+    out = dev.Guarded(out0, "cuda")
+    sc = dev.Guarded(np.zeros(rows, np.float32), "cuda")
+    kvw.kvw_quantize_fp8_rows(out.tensor, sc.tensor, d.tensor, rows=rows, cols=cols,
+                              in_row_stride=in_stride, out_row_stride=out_stride)
+    torch.cuda.synchronize()
+    assert out.guards_intact() and sc.guards_intact()
+    codes, scales = orc.quantize_rows_e4m3(np.ascontiguousarray(x[:, :cols]))
+    got = out.host()
+    assert np.array_equal(sc.host(), scales)
+    assert np.array_equal(got[:, :cols], codes)
+    assert np.array_equal(got[:, cols:], out0[:, cols:])  # the row padding is not written
 
 
 def test_quantize_rows_benchmark_shape(orc, dev):
