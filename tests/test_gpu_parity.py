@@ -282,8 +282,19 @@ def test_knorm_full(orc, dev, G):
     run_knorm(orc, dev, W.knorm_paged(gamma_len=G))
 
 
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_gqa_largest_head(orc, dev, interleaved):
+    """head_size 512 (the largest supported) with 28 + 4 heads: 1024 rotation
+    items per token, the limit of the mrope kernel's one-thread-per-item CTA."""
+    for mode, sec in ((None, None), ("ids", None), ("mrope", (64, 96, 96))):
+        w = W.gqa_workload("big", 450, [3, 0, 9, 1, 20], [0, 5, 40, 31, 7], 28, 4, 512,
+                           page_size=16, freqs_rows=128, base=10000.0, interleaved=interleaved,
+                           position_mode=mode, mrope_section=sec)
+        run_gqa(orc, dev, w)
+
+
 @pytest.mark.parametrize("G,S", [(100, 128), (8, 8), (24, 32), (256, 256), (512, 512),
-                                 (1000, 1024)])
+                                 (1000, 1024), (2048, 2048)])
 def test_knorm_widths(orc, dev, G, S):
     w = W.knorm_workload("w", 600 + G, [2, 0, 30, 1], [5, 0, 13, 61], 3, S, page_size=8,
                          gamma_len=G, spare_pages=2)
@@ -295,6 +306,9 @@ def test_knorm_variants(orc, dev):
                          weight_offset=0.5, multiply_before_cast=False)
     run_knorm(orc, dev, w)
     w = W.knorm_workload("v", 612, [2, 9, 1], [5, 0, 13], 4, 64, page_size=16, gamma_len=256)
+    run_knorm(orc, dev, w, per_head_norm=False)
+    # the widest whole-row norm: 4 heads x 512 = 2048 columns
+    w = W.knorm_workload("v", 613, [2, 9, 1], [5, 0, 13], 4, 512, page_size=16, gamma_len=2048)
     run_knorm(orc, dev, w, per_head_norm=False)
 
 
