@@ -10,7 +10,7 @@
 //
 // GB300 design.  The launch is purely HBM-bound (about 0.5 flop per byte),
 // so the kernel is organised around keeping enough 16-byte loads in flight on
-// all 152 SMs:
+// all SMs:
 //   * CTAs [0, kv_blocks) own latent rows, one warp per token: lane l holds
 //     columns 8l..8l+7 and 256+8l..256+8l+7 of the latent part (lanes 0..7
 //     also one 8-wide slice of the rope part), a 5-step xor-shuffle gives the

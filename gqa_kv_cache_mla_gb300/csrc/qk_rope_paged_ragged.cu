@@ -676,8 +676,13 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     if (a.mode == 2) {
         const uint32_t threads = (uint32_t)((items + 31) / 32 * 32);
         const size_t smem_st = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
+        // small batches: smaller groups, so that every SM gets a few of them
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return KVW_ECUDA;
         int tpb = 4;
-        while (tpb > 1 && (uint64_t)(tot_seq_len + tpb - 1) / tpb < 152ull * 4) tpb >>= 1;
+        while (tpb > 1 && (uint64_t)(tot_seq_len + tpb - 1) / tpb < (uint64_t)sms * 4) tpb >>= 1;
         cudaError_t es;
         auto pick = [&](auto il, auto f8) {
             constexpr bool IL = decltype(il)::value, F8 = decltype(f8)::value;
