@@ -71,6 +71,9 @@ def _load(path):
     L.oracle_mla_gather_latent.restype = u32
     L.oracle_mla_gather_latent.argtypes = [
         vp, i32, f32, vp, i32, f32, vp, u32, u32, u32, u32, i64, i64, i64, u32, vp, u32, u32]
+    L.oracle_mla_gather_latent_dynamic.restype = u32
+    L.oracle_mla_gather_latent_dynamic.argtypes = [
+        vp, vp, vp, i32, f32, vp, u32, u32, u32, u32, i64, i64, i64, u32, vp, u32, u32]
     L.oracle_qk_rope_paged_ragged.restype = u32
     L.oracle_qk_rope_paged_ragged.argtypes = [
         vp, vp, u32, u32, u32, vp, i32, f32, vp, u32, vp, u32, u32, u32, u32, u32, i64, i64,
@@ -117,7 +120,7 @@ class Variant:
                      "rope_pairs_f32", "rms_inv", "rms_norm_f32", "mla_rope_rmsnorm_quant",
                      "qk_rope_paged_ragged", "rms_norm_kv_cache_paged", "has_openmp",
                      "mla_rope_rmsnorm_inplace", "convert_bf16_to_e4m3", "quantize_rows_e4m3",
-                     "mla_gather_latent", "_q_out_buffer"):
+                     "mla_gather_latent", "mla_gather_latent_dynamic", "_q_out_buffer"):
             fn = g[name]
             setattr(self, name, types.FunctionType(fn.__code__, dict(g, lib=lambda: self._L),
                                                    name, fn.__defaults__, fn.__closure__))
@@ -273,6 +276,23 @@ def mla_gather_latent(cache, layer_idx, ctx_offsets, out_dtype=0, out_scale=1.0,
         _p(cache.page_table), cache.max_pages_per_seq, cache.num_pages, cache.num_layers,
         cache.page_size, s[0], s[2], s[3], layer_idx, _p(off), len(off) - 1, rows)
     return out, int(flags)
+
+
+def mla_gather_latent_dynamic(cache, layer_idx, ctx_offsets, out=None, scales=None):
+    """Paged -> contiguous latent rows with per-row dynamic FP8; returns
+    (codes uint8 [rows, 576], scales f32 [rows], flags)."""
+    off = np.ascontiguousarray(ctx_offsets, dtype=np.uint32)
+    rows = int(off[-1]) if off.size else 0
+    if out is None:
+        out = np.zeros((rows, 576), dtype=np.uint8)
+    if scales is None:
+        scales = np.zeros(rows, dtype=np.float32)
+    s = cache.strides
+    flags = lib().oracle_mla_gather_latent_dynamic(
+        _p(out), _p(scales), _p(cache.data), cache.dtype, cache.scale, _p(cache.page_table),
+        cache.max_pages_per_seq, cache.num_pages, cache.num_layers, cache.page_size, s[0], s[2],
+        s[3], layer_idx, _p(off), len(off) - 1, rows)
+    return out, scales, int(flags)
 
 
 def qk_rope_paged_ragged(w, output=None, cache_data=None, nthreads=1, T=None):

@@ -470,6 +470,51 @@ uint32_t oracle_mla_gather_latent(void* out, int out_dtype, float out_scale, con
     return flags;
 }
 
+/*
+ * The same copy with dynamic per-row FP8 (the quantisation of the FP8
+ * prefill branch with dynamic scaling, one scale per context row): the 576
+ * values of the row as the cache holds them (bf16, or E4M3 times
+ * cache_scale), scale = max|v| / 448 (1 for a row of zeros), codes =
+ * satfinite_rne(v / scale).  Rows without a valid page are not written
+ * (neither their codes nor their scale).  Flags as the plain copy.
+ */
+uint32_t oracle_mla_gather_latent_dynamic(uint8_t* out, float* scales, const void* cache,
+                                          int cache_dtype, float cache_scale,
+                                          const uint32_t* page_table, uint32_t max_pages,
+                                          uint32_t num_pages, uint32_t num_layers,
+                                          uint32_t page_size, int64_t s_page, int64_t s_layer,
+                                          int64_t s_token, uint32_t layer_idx,
+                                          const uint32_t* ctx_offsets, uint32_t B,
+                                          uint32_t rows) {
+    const uint32_t ROW = 576;
+    if (rows == 0) return 0;
+    if (!offsets_valid(ctx_offsets, B, rows)) return ORC_FLAG_OFFSETS;
+    orc_layout L = {num_pages, num_layers, page_size, 1, ROW, max_pages,
+                    s_page, 0, s_layer, s_token, ROW, page_table};
+    uint32_t flags = 0;
+    float v[576];
+    for (uint32_t b = 0; b < B; ++b) {
+        for (uint32_t r = ctx_offsets[b]; r < ctx_offsets[b + 1]; ++r) {
+            uint64_t pos = r - ctx_offsets[b];
+            uint32_t f = 0;
+            int64_t base = slot_base(&L, b, pos, layer_idx, &f);
+            flags |= f;
+            if (base < 0) continue;
+            float amax = 0.0f;
+            for (uint32_t j = 0; j < ROW; ++j) {
+                v[j] = load_elem(cache, base + j, cache_dtype, cache_scale);
+                float a = fabsf(v[j]);
+                if (a > amax) amax = a;
+            }
+            float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[r] = sc;
+            for (uint32_t j = 0; j < ROW; ++j)
+                out[(int64_t)r * ROW + j] = oracle_f32_to_e4m3(v[j] / sc);
+        }
+    }
+    return flags;
+}
+
 /* -------------------------------------------------------------- GQA path */
 
 /* Position used for rotary pair k of token t (cache slot position pos_s when

@@ -61,6 +61,12 @@ MUTANTS = [
      "float a = oracle_bf16_to_f32(in[r * in_stride + c]);"),
     ("gather position off by one", "uint64_t pos = r - ctx_offsets[b];",
      "uint64_t pos = r - ctx_offsets[b] + 1;"),
+    ("dynamic gather ignores the cache scale",
+     "v[j] = load_elem(cache, base + j, cache_dtype, cache_scale);",
+     "v[j] = load_elem(cache, base + j, cache_dtype, 1.0f);"),
+    ("dynamic gather multiplies by its scale",
+     "out[(int64_t)r * ROW + j] = oracle_f32_to_e4m3(v[j] / sc);",
+     "out[(int64_t)r * ROW + j] = oracle_f32_to_e4m3(v[j] * sc);"),
     ("offsets order unchecked", "if (offsets[b] > offsets[b + 1]) return 0;",
      "if (0) return 0;"),
     ("page id range unchecked", "if (page >= L->num_pages) {", "if (page == 0xffffffffu) {"),
@@ -98,6 +104,7 @@ PINS = [
     (X.test_gather_fp8_cache_scale, {}),
     (R.test_gqa_fp8_k_vs_complex_fp64, {"interleaved": False}),
     (R.test_gqa_fp8_k_scale_convention, {}),
+    (X.test_gather_dynamic_closed_form_fp8_cache, {}),
 ] + [(R.test_gqa_q_and_k_vs_complex_fp64, {"interleaved": i, "mode": m})
      for i in (True, False) for m in (None, "ids", "mrope")]
 

@@ -169,3 +169,51 @@ def test_gather_fp8_cache_scale(orc):
     assert flags == 0
     for r, raw in _expected_rows(w, ctx).items():
         assert np.array_equal(bf16_to_f32(out[r]), orc.e4m3_decode(raw) * np.float32(2.0))
+
+
+# ------------------------------------------------------------ gather with dynamic per-row FP8
+
+def test_gather_dynamic_equals_gather_then_row_quantisation(orc):
+    """bf16 cache: the fused copy + per-row dynamic FP8 equals the plain copy
+    (bf16 out, an exact copy) followed by the per-row quantiser, codes and
+    scales bit for bit."""
+    w, ctx = _gather_case(W.DTYPE_BF16)
+    rows, flags = orc.mla_gather_latent(w.cache, w.layer_idx, ctx, out_dtype=W.DTYPE_BF16)
+    want_codes, want_scales = orc.quantize_rows_e4m3(rows)
+    codes, scales, f2 = orc.mla_gather_latent_dynamic(w.cache, w.layer_idx, ctx)
+    assert flags == f2 == 0
+    assert np.array_equal(scales, want_scales)
+    assert np.array_equal(codes, want_codes)
+
+
+def test_gather_dynamic_closed_form_fp8_cache(orc):
+    """FP8 cache with scale 0.75: each row's values are code x 0.75, its scale
+    is max|value| / 448, its largest magnitude becomes +-448 and every code is
+    torch's E4M3 cast of value / scale."""
+    w, ctx = _gather_case(W.DTYPE_FP8_E4M3, scale=0.75)
+    codes, scales, flags = orc.mla_gather_latent_dynamic(w.cache, w.layer_idx, ctx)
+    assert flags == 0
+    for r, raw in _expected_rows(w, ctx).items():
+        v = orc.e4m3_decode(raw) * np.float32(0.75)
+        amax = np.float32(np.abs(v).max())
+        assert scales[r] == np.float32(amax / np.float32(448.0))
+        assert np.array_equal(codes[r], _torch_e4m3(v / scales[r]))
+        assert np.abs(orc.e4m3_decode(codes[r])).max() == 448.0
+
+
+def test_gather_dynamic_flags_and_zero_rows(orc):
+    w, ctx = _gather_case(W.DTYPE_BF16)
+    c = w.cache
+    v = c.view6()
+    page = int(c.page_table[3, 0])
+    v[page, 0, w.layer_idx, 0, 0, :] = 0  # request 3's first row: all zeros -> scale 1
+    c.page_table[1, 0] = W.PAGE_UNMAPPED
+    codes, scales, flags = orc.mla_gather_latent_dynamic(w.cache, w.layer_idx, ctx)
+    assert flags == orc.FLAG_PAGE
+    assert not codes[int(ctx[1]):int(ctx[2])].any() and not scales[int(ctx[1]):int(ctx[2])].any()
+    r0 = int(ctx[3])
+    assert scales[r0] == 1.0 and not codes[r0].any()
+    bad = ctx.copy()
+    bad[2] = bad[1] - 1
+    codes, scales, flags = orc.mla_gather_latent_dynamic(w.cache, w.layer_idx, bad)
+    assert flags == orc.FLAG_OFFSETS and not codes.any() and not scales.any()
