@@ -83,9 +83,11 @@ def measured_peak():
 
 
 def source_hash(kernel_file):
+    """Hash of a kernel's source and of every shared device header."""
+    csrc = os.path.join(ROOT, "gqa_kv_cache_mla_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (kernel_file, "kvw_device.cuh"):
-        h.update(open(os.path.join(ROOT, "gqa_kv_cache_mla_gb300", "csrc", f), "rb").read())
+    for f in [kernel_file] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -135,7 +137,7 @@ def algorithmic_bytes(w, name=None):
         return W.algorithmic_bytes_knorm(w.T, c.num_heads, w.gamma.size)
     if k == "gather":
         out_b = 2 if w.out_dtype == W.DTYPE_BF16 else 1
-        return w.rows * W.MLA_ROW * (w.cache.elem_bytes + out_b)
+        return w.rows * (W.MLA_ROW * (w.cache.elem_bytes + out_b) + (4 if w.dynamic else 0))
     if w.per_row:
         return w.x.size * 3 + w.x.shape[0] * 4
     return w.x.size * 3
@@ -223,8 +225,11 @@ def cpu_baseline(w, name, budget_s, single_thread=True):
         fn = lambda: oracle.rms_norm_kv_cache_paged(w, cache_data=cache, nthreads=threads)
     elif k == "gather":
         threads = 1
-        fn = lambda: oracle.mla_gather_latent(w.cache, w.layer_idx, w.ctx_offsets, w.out_dtype,
-                                              w.out_scale)
+        if w.dynamic:
+            fn = lambda: oracle.mla_gather_latent_dynamic(w.cache, w.layer_idx, w.ctx_offsets)
+        else:
+            fn = lambda: oracle.mla_gather_latent(w.cache, w.layer_idx, w.ctx_offsets,
+                                                  w.out_dtype, w.out_scale)
     else:
         threads = 1
         fn = ((lambda: oracle.quantize_rows_e4m3(w.x)) if w.per_row

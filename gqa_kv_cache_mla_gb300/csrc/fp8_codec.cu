@@ -59,22 +59,12 @@ __global__ void __launch_bounds__(kThreads) convert_kernel(uint2* out, const uin
     }
 }
 
-// x / s for the quantiser, from y = RN(1/s): see the file comment for the
-// method and its range.  copysignf keeps the sign of x on a zero result.
-__device__ __forceinline__ float div_refined(float x, float s, float y) {
-    const float q0 = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q0, s, x);
-    return copysignf(__fmaf_rn(r, y, q0), x);
-}
-
 // Scale of a row: max|x| / 448, or 1 for a row of zeros.
 __device__ __forceinline__ float row_scale(float amax) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
 }
-
-__device__ __forceinline__ bool refined_ok(float sc) { return sc >= 0x1p-60f && sc <= 0x1p60f; }
 
 template <bool REFINED>
 __device__ __forceinline__ uint2 quantize8(const uint4& v, float sc, float y) {

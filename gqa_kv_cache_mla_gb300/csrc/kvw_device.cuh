@@ -129,6 +129,23 @@ __device__ __forceinline__ float rms_inv(float ss, float n, float eps) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), eps)));
 }
 
+// x / s for the dynamic FP8 quantisers, from y = RN(1/s) and one FMA
+// correction step (Markstein's division refinement: P. Markstein, IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(x*y), r = x - q0*s (exact with an FMA),
+// q = RN(q0 + r*y), the correctly rounded quotient while s, 1/s and the
+// remainder are normal.  Used for scales in [2^-60, 2^60] (refined_ok) on
+// bf16 values x with s = RN(amax / 448), amax a bf16 magnitude, where every
+// quotient of magnitude >= 2^-14 keeps all three normal and smaller ones give
+// an E4M3 zero whatever their last bits; copysignf keeps the sign of x on a
+// zero result.
+__device__ __forceinline__ float div_refined(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, s, x);
+    return copysignf(__fmaf_rn(r, y, q0), x);
+}
+
+__device__ __forceinline__ bool refined_ok(float sc) { return sc >= 0x1p-60f && sc <= 0x1p60f; }
+
 __device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
     if (err_flags) atomicOr(err_flags, bits);
 }

@@ -134,6 +134,117 @@ __global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherArgs a)
     }
 }
 
+// Copy with dynamic per-row FP8.  A row's scale needs all of its 576 values,
+// so here a warp owns whole rows, kDynRows at a time (lane l holds pieces l,
+// l + 32 and, for l < 8, l + 64 of each): the row maxima are warp shuffles,
+// the scale and its reciprocal are computed in registers and every piece is
+// quantised from the registers that still hold it -- no shared-memory
+// reduction and no block barrier after the offsets are staged.  Warps are
+// persistent; lane q < kDynRows resolves the page of row q of the warp's next
+// step while the current step's loads are in flight.  Values that are bf16
+// numbers (a bf16 cache, or E4M3 codes at cache scale 1) divide by the scale
+// through div_refined; others through the IEEE divide.
+constexpr uint32_t kDynRows = 4;
+
+// base[i] for a run-time i < kDynRows, without indexing registers dynamically
+__device__ __forceinline__ int64_t base_of(const int64_t (&base)[kDynRows], uint32_t i) {
+    int64_t b = base[0];
+#pragma unroll
+    for (uint32_t q = 1; q < kDynRows; ++q) b = i == q ? base[q] : b;
+    return b;
+}
+
+template <bool CF8>
+__global__ void __launch_bounds__(kThreads, 3) gather_dynamic_kernel(const GatherArgs a,
+                                                                     float* scales) {
+    extern __shared__ uint32_t s_off[];
+    int ok = 1;
+    for (uint32_t i = threadIdx.x; i <= a.B; i += blockDim.x) {
+        const uint32_t o = __ldg(a.ctx_offsets + i);
+        s_off[i] = o;
+        if (i < a.B && o > __ldg(a.ctx_offsets + i + 1)) ok = 0;
+        if ((i == 0 && o != 0u) || (i == a.B && o != a.rows)) ok = 0;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t nwarps = gridDim.x * (kThreads / 32);
+    const uint32_t steps = (a.rows + kDynRows - 1) / kDynRows;
+    uint32_t st = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    int64_t base_lane = (st < steps && lane < kDynRows) ? row_base(a, s_off, st * kDynRows + lane)
+                                                         : -1;
+    const bool bf16_values = !CF8 || a.cache_scale == 1.0f;
+    for (; st < steps; st += nwarps) {
+        int64_t base[kDynRows];
+        uint4 raw[kDynRows][3];
+#pragma unroll
+        for (uint32_t q = 0; q < kDynRows; ++q) {
+            base[q] = __shfl_sync(0xffffffffu, base_lane, q);
+            if (base[q] >= 0) {
+                raw[q][0] = load_raw8<CF8>(a.cache, base[q] + lane * 8);
+                raw[q][1] = load_raw8<CF8>(a.cache, base[q] + 256 + lane * 8);
+                if (lane < 8) raw[q][2] = load_raw8<CF8>(a.cache, base[q] + 512 + lane * 8);
+            }
+        }
+        const uint32_t next = st + nwarps;
+        base_lane = (next < steps && lane < kDynRows) ? row_base(a, s_off, next * kDynRows + lane)
+                                                      : -1;
+        // row maxima: the kDynRows shuffle chains run side by side
+        float m[kDynRows];
+#pragma unroll
+        for (uint32_t q = 0; q < kDynRows; ++q) {
+            m[q] = 0.0f;
+            if (base[q] < 0) continue;
+#pragma unroll
+            for (uint32_t j = 0; j < 3; ++j) {
+                if (j == 2 && lane >= 8) break;
+                float v[8];
+                to_f32<CF8>(raw[q][j], a.cache_scale, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m[q] = fmaxf(m[q], fabsf(v[e]));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (uint32_t q = 0; q < kDynRows; ++q)
+                m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
+        }
+        // lane q turns row q's maximum into its scale and reciprocal
+        float mine = m[0];
+#pragma unroll
+        for (uint32_t q = 1; q < kDynRows; ++q) mine = lane == q ? m[q] : mine;
+        const float sc_lane = mine > 0.0f ? __fdiv_rn(mine, 448.0f) : 1.0f;
+        const float y_lane = __frcp_rn(sc_lane);
+        if (lane < kDynRows && base_of(base, lane) >= 0)
+            scales[(uint64_t)st * kDynRows + lane] = sc_lane;
+#pragma unroll
+        for (uint32_t q = 0; q < kDynRows; ++q) {
+            const float sc = __shfl_sync(0xffffffffu, sc_lane, q);
+            const float y = __shfl_sync(0xffffffffu, y_lane, q);
+            if (base[q] < 0) continue;  // warp-uniform
+            const uint64_t r = (uint64_t)st * kDynRows + q;
+            const bool fast = bf16_values && refined_ok(sc);
+#pragma unroll
+            for (uint32_t j = 0; j < 3; ++j) {
+                if (j == 2 && lane >= 8) break;
+                float v[8];
+                to_f32<CF8>(raw[q][j], a.cache_scale, v);
+                if (fast) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = div_refined(v[e], sc, y);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(v[e], sc);
+                }
+                *reinterpret_cast<uint2*>(a.out + r * kRow + 256u * j + lane * 8) = pack8_e4m3(v);
+            }
+        }
+    }
+}
+
 template <bool CF8, bool OF8>
 cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
     auto k = gather_kernel<CF8, OF8>;
@@ -153,37 +264,44 @@ cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <bool CF8>
+cudaError_t launch_dynamic(const GatherArgs& a, float* scales, cudaStream_t stream) {
+    auto k = gather_dynamic_kernel<CF8>;
+    const size_t smem = sizeof(uint32_t) * ((size_t)a.B + 1);
+    if (smem > 32 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const uint32_t ctas = (a.rows + kDynRows * (kThreads / 32) - 1) / (kDynRows * (kThreads / 32));
+    const uint32_t wave = (uint32_t)(sms * (per_sm > 0 ? per_sm : 1));
+    k<<<ctas < wave ? ctas : wave, kThreads, smem, stream>>>(a, scales);
+    return cudaGetLastError();
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-}  // namespace
-}  // namespace kvw
-
-extern "C" int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_scale,
-                                     const kvw_paged_cache_t* cache, uint32_t layer_idx,
-                                     const uint32_t* ctx_offsets, uint32_t num_batches,
-                                     uint32_t total_rows, uint32_t* err_flags,
-                                     cudaStream_t stream) {
-    using namespace kvw;
-    if (!cache) return KVW_EINVAL;
-    if (out_dtype != KVW_DTYPE_BF16 && out_dtype != KVW_DTYPE_FP8_E4M3) return KVW_EUNSUPPORTED;
+// Host checks shared by both entry points; fills `a` (out left null).
+int make_args(const kvw_paged_cache_t* cache, uint32_t layer_idx, const uint32_t* ctx_offsets,
+              uint32_t num_batches, uint32_t total_rows, uint32_t* err_flags, GatherArgs& a) {
     if (cache->dtype != KVW_DTYPE_BF16 && cache->dtype != KVW_DTYPE_FP8_E4M3) return KVW_EUNSUPPORTED;
     if (cache->head_size != kRow || cache->num_heads != 1) return KVW_EUNSUPPORTED;
     if (num_batches > KVW_MAX_BATCHES) return KVW_EUNSUPPORTED;
-    if (total_rows == 0) return KVW_OK;
-    const bool cf8 = cache->dtype == KVW_DTYPE_FP8_E4M3, of8 = out_dtype == KVW_DTYPE_FP8_E4M3;
+    const bool cf8 = cache->dtype == KVW_DTYPE_FP8_E4M3;
     const int64_t esz = cf8 ? 1 : 2;
-    if (!out || !ctx_offsets || !cache->data || !cache->page_table) return KVW_EINVAL;
+    if (!ctx_offsets || !cache->data || !cache->page_table) return KVW_EINVAL;
     if (layer_idx >= cache->num_layers || cache->page_size == 0 || cache->max_pages_per_seq == 0)
         return KVW_EINVAL;
-    if ((cf8 && !(cache->scale > 0.0f && cache->scale < 3.0e38f)) ||
-        (of8 && !(out_scale > 0.0f && out_scale < 3.0e38f)))
-        return KVW_EINVAL;
-    if (!aligned16(out) || !aligned16(cache->data)) return KVW_EINVAL;
+    if (cf8 && !(cache->scale > 0.0f && cache->scale < 3.0e38f)) return KVW_EINVAL;
+    if (!aligned16(cache->data)) return KVW_EINVAL;
     if ((cache->stride_page * esz) % 16 || (cache->stride_layer * esz) % 16 ||
         (cache->stride_token * esz) % 16 || cache->stride_page <= 0 || cache->stride_token <= 0)
         return KVW_EINVAL;
-    GatherArgs a;
-    a.out = static_cast<unsigned char*>(out);
+    a.out = nullptr;
     a.cache = static_cast<const unsigned char*>(cache->data);
     a.ctx_offsets = ctx_offsets;
     a.page_table = cache->page_table;
@@ -197,8 +315,52 @@ extern "C" int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_sca
     a.num_pages = cache->num_pages;
     a.page_size = cache->page_size;
     a.cache_scale = cache->scale;
+    a.out_scale = 1.0f;
+    return KVW_OK;
+}
+
+}  // namespace
+}  // namespace kvw
+
+extern "C" int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_scale,
+                                     const kvw_paged_cache_t* cache, uint32_t layer_idx,
+                                     const uint32_t* ctx_offsets, uint32_t num_batches,
+                                     uint32_t total_rows, uint32_t* err_flags,
+                                     cudaStream_t stream) {
+    using namespace kvw;
+    if (!cache) return KVW_EINVAL;
+    if (out_dtype != KVW_DTYPE_BF16 && out_dtype != KVW_DTYPE_FP8_E4M3) return KVW_EUNSUPPORTED;
+    GatherArgs a;
+    const int st = make_args(cache, layer_idx, ctx_offsets, num_batches, total_rows, err_flags, a);
+    if (st != KVW_OK) return st;
+    if (total_rows == 0) return KVW_OK;
+    const bool cf8 = cache->dtype == KVW_DTYPE_FP8_E4M3, of8 = out_dtype == KVW_DTYPE_FP8_E4M3;
+    if (!out || !aligned16(out)) return KVW_EINVAL;
+    if (of8 && !(out_scale > 0.0f && out_scale < 3.0e38f)) return KVW_EINVAL;
+    a.out = static_cast<unsigned char*>(out);
     a.out_scale = out_scale;
     const cudaError_t e = cf8 ? (of8 ? launch<true, true>(a, stream) : launch<true, false>(a, stream))
                               : (of8 ? launch<false, true>(a, stream) : launch<false, false>(a, stream));
+    return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
+}
+
+extern "C" int kvw_mla_gather_latent_fp8_dynamic(void* out_codes, float* out_scales,
+                                                 const kvw_paged_cache_t* cache,
+                                                 uint32_t layer_idx, const uint32_t* ctx_offsets,
+                                                 uint32_t num_batches, uint32_t total_rows,
+                                                 uint32_t* err_flags, cudaStream_t stream) {
+    using namespace kvw;
+    if (!cache) return KVW_EINVAL;
+    GatherArgs a;
+    const int st = make_args(cache, layer_idx, ctx_offsets, num_batches, total_rows, err_flags, a);
+    if (st != KVW_OK) return st;
+    if (total_rows == 0) return KVW_OK;
+    if (!out_codes || !out_scales || !aligned16(out_codes) ||
+        (reinterpret_cast<uintptr_t>(out_scales) & 3u) != 0)
+        return KVW_EINVAL;
+    a.out = static_cast<unsigned char*>(out_codes);
+    const cudaError_t e = cache->dtype == KVW_DTYPE_FP8_E4M3
+                              ? launch_dynamic<true>(a, out_scales, stream)
+                              : launch_dynamic<false>(a, out_scales, stream);
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }

@@ -173,11 +173,16 @@ class DeviceGather(_Base):
         self.out_init = np.zeros((w.rows, 576), np.uint16 if w.out_dtype == W.DTYPE_BF16
                                  else np.uint8)
         self.out = self._g(self.out_init, guard)
+        self.scales = self._g(np.zeros(w.rows, np.float32), guard)
         self.err = self._g(np.zeros(1, np.uint32), guard)
         self.desc = _cache_desc(c, self.cache, self.page_table, self.cache_lengths)
 
     def run(self, stream=None, check=True):
         w = self.w
+        if w.dynamic:
+            return kvw.kvw_mla_gather_latent_fp8_dynamic(
+                self.out.tensor, self.scales.tensor, self.desc, w.layer_idx, self.ctx.tensor,
+                self.err.tensor, stream, total_rows=w.rows, check=check)
         return kvw.kvw_mla_gather_latent(self.out.tensor, w.out_dtype, w.out_scale, self.desc,
                                          w.layer_idx, self.ctx.tensor, self.err.tensor, stream,
                                          total_rows=w.rows, check=check)

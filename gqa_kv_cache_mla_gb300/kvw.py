@@ -75,6 +75,8 @@ def _load():
                                                i32, pc, u32, f32, vp, vp]
     L.kvw_mla_gather_latent.restype = ctypes.c_int
     L.kvw_mla_gather_latent.argtypes = [vp, i32, f32, pc, u32, vp, u32, u32, vp, vp]
+    L.kvw_mla_gather_latent_fp8_dynamic.restype = ctypes.c_int
+    L.kvw_mla_gather_latent_fp8_dynamic.argtypes = [vp, vp, pc, u32, vp, u32, u32, vp, vp]
     L.kvw_convert_bf16_to_fp8_e4m3.restype = ctypes.c_int
     L.kvw_convert_bf16_to_fp8_e4m3.argtypes = [vp, vp, ctypes.c_uint64, f32, vp]
     L.kvw_quantize_fp8_rows.restype = ctypes.c_int
@@ -210,6 +212,17 @@ def kvw_mla_gather_latent(out, out_dtype: int, out_scale: float, cache: PagedCac
                                    layer_idx, _ptr(ctx_offsets), B, rows, _ptr(err_flags),
                                    _stream(stream))
     return _done(st, "kvw_mla_gather_latent", check)
+
+
+def kvw_mla_gather_latent_fp8_dynamic(out_codes, out_scales, cache: PagedCacheT, layer_idx: int,
+                                      ctx_offsets, err_flags=None, stream=None, *,
+                                      num_batches=None, total_rows=None, check=True) -> int:
+    B = ctx_offsets.shape[0] - 1 if num_batches is None else num_batches
+    rows = out_codes.shape[0] if total_rows is None else total_rows
+    st = lib.kvw_mla_gather_latent_fp8_dynamic(_ptr(out_codes), _ptr(out_scales),
+                                               ctypes.byref(cache), layer_idx, _ptr(ctx_offsets),
+                                               B, rows, _ptr(err_flags), _stream(stream))
+    return _done(st, "kvw_mla_gather_latent_fp8_dynamic", check)
 
 
 def kvw_convert_bf16_to_fp8_e4m3(out, inp, scale: float = 1.0, stream=None, *, n=None,

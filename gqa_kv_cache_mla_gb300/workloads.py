@@ -328,6 +328,7 @@ class GatherWorkload:
     ctx_offsets: np.ndarray  # uint32 [B+1] over whole contexts
     out_dtype: int
     out_scale: float
+    dynamic: bool = False  # per-row dynamic FP8 (codes + one scale per row)
 
     @property
     def rows(self):
@@ -338,9 +339,11 @@ class GatherWorkload:
         return self.rows
 
 
-def mla_gather(w: MLAWorkload, out_dtype=DTYPE_FP8_E4M3, out_scale=1.0, seed=9) -> GatherWorkload:
+def mla_gather(w: MLAWorkload, out_dtype=DTYPE_FP8_E4M3, out_scale=1.0, seed=9,
+               dynamic=False) -> GatherWorkload:
     ctx = fill_contexts(rng_for(seed), w.cache, w.offsets, w.layer_idx)
-    return GatherWorkload(w.name + "_gather", w.cache, w.layer_idx, ctx, out_dtype, out_scale)
+    return GatherWorkload(w.name + "_gather", w.cache, w.layer_idx, ctx,
+                          DTYPE_FP8_E4M3 if dynamic else out_dtype, out_scale, dynamic)
 
 
 @dataclasses.dataclass
@@ -553,6 +556,11 @@ REGISTRY = {
                            "mla_gather_latent.cu",
                            "paged->contiguous latent gather of the prefill contexts, bf16 "
                            "cache to FP8 E4M3 (scale 1)"),
+    "mla_gather_prefill_dynamic": (lambda s: mla_gather(mla_prefill(DTYPE_BF16, seed=s + 1),
+                                                       dynamic=True),
+                                   "mla_gather_latent.cu",
+                                   "paged->contiguous latent gather of the prefill contexts, bf16 "
+                                   "cache to FP8 E4M3 with a dynamic scale per row"),
     "fp8_convert": (lambda s: fp8_convert(seed=s + 10), "fp8_codec.cu",
                     "bf16 -> E4M3 conversion of 2^26 values"),
     "fp8_quant_rows": (lambda s: fp8_quant_rows(seed=s + 11), "fp8_codec.cu",

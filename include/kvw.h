@@ -195,6 +195,29 @@ int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_scale,
                           uint32_t* err_flags, cudaStream_t stream);
 
 /*
+ * The same copy quantised with dynamic FP8 scaling, one scale per row (the
+ * "mla_graph" module page: entry mla_prefill_branch_fp8 copies the KV latent
+ * values out of the paged cache and quantises them to FP8; the module
+ * description names dynamic FP8 scaling).  For each context row r, with v
+ * its 576 values as the cache holds them (bf16, or E4M3 times the cache
+ * scale):
+ *   out_scales[r] = max_j |v_j| / 448   (1 for an all-zero row)
+ *   out_codes[r][j] = satfinite_round_nearest_even(v_j / out_scales[r])
+ * One pass over the cache: equal, codes and scales, to kvw_mla_gather_latent
+ * to bf16 followed by kvw_quantize_fp8_rows for a bf16 cache.
+ *
+ *   out_codes    device, uint8 [total_rows, 576], 16-byte aligned
+ *   out_scales   device, f32 [total_rows]
+ *   other arguments, flags and errors as kvw_mla_gather_latent; a row
+ *   without a valid page is not written (neither codes nor scale).
+ */
+int kvw_mla_gather_latent_fp8_dynamic(void* out_codes, float* out_scales,
+                                      const kvw_paged_cache_t* cache, uint32_t layer_idx,
+                                      const uint32_t* ctx_offsets, uint32_t num_batches,
+                                      uint32_t total_rows, uint32_t* err_flags,
+                                      cudaStream_t stream);
+
+/*
  * bf16 -> FP8 E4M3 ("mla_graph" module page, convert_bf16_to_fp8_e4m3fn):
  * out[i] = satfinite_round_nearest_even(in[i] / scale), n a multiple of 8.
  *   out  device, n bytes, 8-byte aligned;  in  device, n bf16, 16-byte aligned

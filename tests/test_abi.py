@@ -17,7 +17,8 @@ def test_exports_every_header_function():
     names = kvw.header_functions()
     assert set(names) == {"kvw_mla_rope_rmsnorm_quant", "kvw_mla_rope_rmsnorm_inplace",
                           "kvw_qk_rope_paged_ragged", "kvw_rms_norm_kv_cache_paged",
-                          "kvw_mla_gather_latent", "kvw_convert_bf16_to_fp8_e4m3",
+                          "kvw_mla_gather_latent", "kvw_mla_gather_latent_fp8_dynamic",
+                          "kvw_convert_bf16_to_fp8_e4m3",
                           "kvw_quantize_fp8_rows", "kvw_status_string", "kvw_version"}
     for n in names:
         assert hasattr(kvw.lib, n)
@@ -207,3 +208,16 @@ def test_binding_output_type_follows_the_buffer():
         kvw._out_dtype(u8, kvw.DTYPE_BF16, "x")
     with pytest.raises(ValueError):
         kvw._out_dtype(i16, kvw.DTYPE_FP8_E4M3, "x")
+
+
+def test_gather_dynamic_host_checks():
+    c = _mla_cache()
+    f = kvw.lib.kvw_mla_gather_latent_fp8_dynamic
+    assert f(FAKE, FAKE, ctypes.byref(c), 1, FAKE, 2, 0, None, 0) == kvw.KVW_OK
+    assert f(ODD, FAKE, ctypes.byref(c), 1, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    assert f(FAKE, FAKE + 2, ctypes.byref(c), 1, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    assert f(FAKE, None, ctypes.byref(c), 1, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    assert f(FAKE, FAKE, ctypes.byref(c), 2, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    assert f(FAKE, FAKE, None, 1, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
+    c2 = _mla_cache(head_size=512)
+    assert f(FAKE, FAKE, ctypes.byref(c2), 1, FAKE, 2, 8, None, 0) == kvw.KVW_EUNSUPPORTED

@@ -477,6 +477,16 @@ def run_gather(orc, dev, g):
     d = dev.DeviceGather(g)
     d.run()
     torch.cuda.synchronize()
+    if g.dynamic:
+        ref, ref_scales, f_ref = orc.mla_gather_latent_dynamic(
+            g.cache, g.layer_idx, g.ctx_offsets, out=d.out_init.copy(),
+            scales=np.zeros(g.rows, np.float32))
+        assert d.guards_intact()
+        assert d.flags() == f_ref
+        assert np.array_equal(d.scales.host(), ref_scales)
+        assert np.array_equal(d.out.host(), ref)
+        assert np.array_equal(d.cache.host(), g.cache.data)
+        return d
     ref, f_ref = orc.mla_gather_latent(g.cache, g.layer_idx, g.ctx_offsets, g.out_dtype,
                                        g.out_scale, out=d.out_init.copy())
     assert d.guards_intact()
@@ -502,6 +512,50 @@ def test_gather_small(orc, dev, src, dst):
 @pytest.mark.parametrize("dst", [W.DTYPE_FP8_E4M3, W.DTYPE_BF16])
 def test_gather_prefill_full(orc, dev, dst):
     run_gather(orc, dev, W.mla_gather(W.mla_prefill(W.DTYPE_BF16), out_dtype=dst))
+
+
+@pytest.mark.parametrize("src,scale", [(W.DTYPE_BF16, 1.0), (W.DTYPE_FP8_E4M3, 1.0),
+                                       (W.DTYPE_FP8_E4M3, 0.625)])
+def test_gather_dynamic_small(orc, dev, src, scale):
+    """Codes and scales bit for bit: bf16 values and FP8 at scale 1 take the
+    reciprocal-and-FMA division, FP8 at another scale the IEEE divide."""
+    w = W.mla_workload("g", 860, [3, 0, 17, 1, 40, 70], [5, 9, 100, 31, 0, 200], num_heads=1,
+                       page_size=16, max_seq_len=512, cache_dtype=src, num_layers=2,
+                       layer_idx=1, scale=scale)
+    g = W.mla_gather(w, dynamic=True)
+    run_gather(orc, dev, g)
+
+
+def test_gather_dynamic_outliers_and_zero_rows(orc, dev):
+    """Rows with x1000 outliers (tiny quotients elsewhere in the row) and an
+    all-zero row (scale 1)."""
+    w = W.mla_workload("g", 861, [30, 50], [10, 0], num_heads=1, page_size=16, max_seq_len=128,
+                       cache_dtype=W.DTYPE_BF16)
+    g = W.mla_gather(w, dynamic=True)
+    v = g.cache.view6()
+    rng = np.random.default_rng(862)
+    for b in range(2):
+        for p in range(int(g.ctx_offsets[b + 1] - g.ctx_offsets[b])):
+            page = int(g.cache.page_table[b, p // 16])
+            row = v[page, 0, g.layer_idx, p % 16, 0]
+            if p == 3:
+                row[:] = 0
+            elif p % 4 == 1:
+                big = np.array([1000.0 * (1 + rng.random())], np.float32)
+                row[rng.integers(0, 576)] = W.bf16_bits(big)[0]
+    run_gather(orc, dev, g)
+
+
+def test_gather_dynamic_prefill_full(orc, dev):
+    run_gather(orc, dev, W.REGISTRY["mla_gather_prefill_dynamic"][0](2))
+
+
+def test_gather_dynamic_flags(orc, dev):
+    w = W.mla_workload("g", 863, [3, 5], [0, 7], num_heads=1, page_size=16, max_seq_len=64,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    g = W.mla_gather(w, dynamic=True)
+    g.cache.page_table[1, 0] = W.PAGE_UNMAPPED
+    assert run_gather(orc, dev, g).flags() == 1
 
 
 def test_gather_decode_contexts(orc, dev):
