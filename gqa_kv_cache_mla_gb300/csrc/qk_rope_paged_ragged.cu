@@ -389,9 +389,17 @@ cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
 // double-buffered shared area -- slot rows and position checks (one thread
 // per token) and the composed (cos, sin) row of each token (all threads,
 // one pair each) -- then rotates and stores the group in hand.
+// Composed (cos, sin) rows are stored swizzled: float4 q (pairs 8m + 2q and
+// 8m + 2q + 1) of pair group m sits in slot (q + m / 2) mod 4 of the group's
+// four, so when the 8 lanes of a quarter-warp (m = 0..7) read their float4 q
+// they touch 8 different 16-byte bank groups instead of 2.
+__device__ __forceinline__ uint32_t cs_slot(uint32_t m, uint32_t q) {
+    return 16u * m + 4u * ((q + (m >> 1)) & 3u);
+}
+
 template <int TPB>
 struct StagedSmem {
-    float cs[2][TPB][kMaxHead];  // composed (cos, sin) per pair
+    float cs[2][TPB][kMaxHead];  // composed (cos, sin) per pair, swizzled (cs_slot)
     int64_t kbase[2][TPB];       // slot row of each token (-1: no page)
     int bad[2][TPB];             // a RoPE position of the token is out of range
 };
@@ -441,7 +449,7 @@ __device__ __forceinline__ void staged_prepare(const GqaArgs& a, const uint32_t*
         }
         float2 cs = make_float2(0.f, 0.f);
         if (p < a.freqs_rows) cs = __ldg(reinterpret_cast<const float2*>(a.freqs + p * a.S) + k);
-        *reinterpret_cast<float2*>(&sm.cs[buf][u][2 * k]) = cs;
+        *reinterpret_cast<float2*>(&sm.cs[buf][u][cs_slot(k >> 3, (k >> 1) & 3u) + 2u * (k & 1u)]) = cs;
     }
 }
 
@@ -514,8 +522,11 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
                 const uint32_t t = t_begin + u;
                 if (t >= a.T || sm.bad[buf][u]) continue;
                 if (!is_q && sm.kbase[buf][u] < 0) continue;
-                const float4* cs4 = reinterpret_cast<const float4*>(&sm.cs[buf][u][16u * m]);
-                const float4 c0 = cs4[0], c1 = cs4[1], c2 = cs4[2], c3 = cs4[3];
+                const float* row = sm.cs[buf][u];
+                const float4 c0 = *reinterpret_cast<const float4*>(row + cs_slot(m, 0));
+                const float4 c1 = *reinterpret_cast<const float4*>(row + cs_slot(m, 1));
+                const float4 c2 = *reinterpret_cast<const float4*>(row + cs_slot(m, 2));
+                const float4 c3 = *reinterpret_cast<const float4*>(row + cs_slot(m, 3));
                 const float c[8] = {c0.x, c0.z, c1.x, c1.z, c2.x, c2.z, c3.x, c3.z};
                 const float s[8] = {c0.y, c0.w, c1.y, c1.w, c2.y, c2.w, c3.y, c3.w};
                 float va[8], vb[8], ya[8], yb[8];
