@@ -253,10 +253,33 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
             float c[8], sn[8];
             const float* frow = reinterpret_cast<const float*>(st + a.f_off) + (size_t)u * a.R * a.S;
             if (a.mode != 2) {
+                // The 8 lanes of a quarter-warp (m = 0..7) would read their
+                // float4 q at 64 m + 16 q: 2 bank groups, 4-way conflicts.
+                // Lane m reads them rotated by r = m / 2 (8 distinct bank
+                // groups per load) and rotates them back with selects.
                 const float4* f4 = reinterpret_cast<const float4*>(frow + 16u * m);
+                const uint32_t r = (m >> 1) & 3u;
+                float4 t[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) t[q] = f4[(q + r) & 3u];
+                if (r & 1u) {  // rotate right by one
+                    const float4 x = t[3];
+                    t[3] = t[2];
+                    t[2] = t[1];
+                    t[1] = t[0];
+                    t[0] = x;
+                }
+                if (r & 2u) {  // rotate right by two
+                    float4 x = t[0];
+                    t[0] = t[2];
+                    t[2] = x;
+                    x = t[1];
+                    t[1] = t[3];
+                    t[3] = x;
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float4 v = f4[q];
+                    const float4 v = t[q];
                     c[2 * q] = v.x;
                     sn[2 * q] = v.y;
                     c[2 * q + 1] = v.z;
