@@ -15,9 +15,9 @@
 //   * A producer warp resolves each group's tokens (request by binary search
 //     in the staged offsets, slot position, RoPE positions, page id) and
 //     issues bulk (TMA) copies into a 2-stage shared-memory ring: the group's
-//     q_proj rows (one copy, they are contiguous), each token's K rows (one
-//     copy when the kv heads are contiguous) and the spans of freqs_cis rows
-//     the token's pairs use (one row, or the three mrope rows' sections).
+//     q_proj rows (one copy, they are contiguous), the K rows (one copy per
+//     run of adjacent slots) and the freqs_cis rows (one copy per run of
+//     consecutive positions, or one per token with position_ids).
 //     Copies complete on the stage's "full" mbarrier with a transaction
 //     count, so no thread waits on individual loads.
 //   * Twelve consumer warps (more measured no better, eight 2-4% slower) wait
@@ -64,8 +64,6 @@ struct GqaArgs {
     uint32_t B, T, Hq, Hk, S, freqs_rows, max_pages, num_pages, page_size;
     uint32_t mode;              // 0: slot positions, 1: position_ids[T], 2: mrope [3, T]
     uint32_t sec0, sec01;       // mrope section ends, in pairs
-    uint32_t R;                 // freqs rows kept per token (1, or 3 for mrope)
-    uint32_t span_lo[3], span_hi[3];  // pair span copied from each row (even bounds)
     uint32_t tpb, groups;       // tokens per group, number of groups
     uint32_t heads_contig;      // kv heads adjacent (stride_head == S)
     uint32_t rows_contig;       // token rows adjacent too (stride_token == Hk * S)
@@ -77,6 +75,11 @@ struct GqaArgs {
 
 __device__ __forceinline__ uint32_t section_of(const GqaArgs& a, uint32_t k) {
     return k < a.sec0 ? 0u : (k < a.sec01 ? 1u : 2u);
+}
+
+// Whether mrope position row r supplies any pair (its section is not empty).
+__device__ __forceinline__ bool section_used(const GqaArgs& a, uint32_t r) {
+    return r == 0 ? a.sec0 > 0u : (r == 1 ? a.sec01 > a.sec0 : (a.S >> 1) > a.sec01);
 }
 
 struct TokMeta {
@@ -106,36 +109,22 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
         }
         const uint32_t t0 = g * a.tpb;
         const uint32_t ntok = min(a.tpb, a.T - t0);
-        uint64_t p[3] = {0, 0, 0};
+        uint64_t p = 0;  // RoPE position: the slot position, or position_ids[t]
         int64_t kbase = -1;
         uint32_t qok = 0, bytes = 0;
         if (lane < ntok) {
             const uint32_t t = t0 + lane;
             const uint32_t b = find_request(s_off, a.B, t);
             const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-            qok = 1;
-            if (a.mode == 0) {
-                p[0] = pos;
-                qok = pos < a.freqs_rows;
-            } else if (a.mode == 1) {
-                p[0] = __ldg(a.position_ids + t);
-                qok = p[0] < a.freqs_rows;
-            } else {
-#pragma unroll
-                for (int r = 0; r < 3; ++r) {
-                    if (a.span_hi[r] > a.span_lo[r]) {
-                        p[r] = __ldg(a.position_ids + (uint64_t)r * a.T + t);
-                        if (p[r] >= a.freqs_rows) qok = 0;
-                    }
-                }
-            }
+            p = a.mode == 0 ? pos : (uint64_t)__ldg(a.position_ids + t);
+            qok = p < a.freqs_rows;
             if (!qok) {
                 flag(a.err_flags, KVW_ERR_POSITION);
             } else {
                 kbase = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
                                  a.s_token, a.layer_off, b, pos);
                 if (kbase < 0) flag(a.err_flags, KVW_ERR_PAGE);
-                for (uint32_t r = 0; r < a.R; ++r) bytes += (a.span_hi[r] - a.span_lo[r]) * 8u;
+                bytes += a.S * 4u;  // the freqs row
                 if (kbase >= 0) bytes += a.Hk * krow_bytes;
             }
         }
@@ -167,10 +156,10 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
         const bool kcont = a.rows_contig && lane > 0 && lane < ntok && qok && kbase >= 0 &&
                            kprev >= 0 && kbase == kprev + a.s_token;
         const uint32_t kstarts = __ballot_sync(0xffffffffu, lane < ntok && qok && kbase >= 0 && !kcont);
-        const uint64_t pprev = __shfl_up_sync(0xffffffffu, p[0], 1);
+        const uint64_t pprev = __shfl_up_sync(0xffffffffu, p, 1);
         const uint32_t qok_mask = __ballot_sync(0xffffffffu, lane < ntok && qok);
         const bool fcont = a.mode == 0 && lane > 0 && lane < ntok && qok &&
-                           ((qok_mask >> (lane - 1)) & 1u) && p[0] == pprev + 1;
+                           ((qok_mask >> (lane - 1)) & 1u) && p == pprev + 1;
         const uint32_t fstarts = __ballot_sync(0xffffffffu, lane < ntok && qok && !fcont);
         if (lane < ntok && qok) {
             if (kbase >= 0 && !kcont) {
@@ -190,22 +179,13 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
                                   krow_bytes, &full[s]);
                 }
             }
-            if (a.mode == 0) {
-                if (!fcont) {
-                    uint32_t n = 1;
-                    while (lane + n < ntok && ((fstarts >> (lane + n)) & 1u) == 0u &&
-                           ((qok_mask >> (lane + n)) & 1u))
-                        ++n;
-                    bulk_load(st + a.f_off + (size_t)lane * a.R * a.S * 4u, a.freqs + p[0] * a.S,
-                              n * a.S * 4u, &full[s]);
-                }
-            } else {
-                for (uint32_t r = 0; r < a.R; ++r) {
-                    const uint32_t lo = a.span_lo[r], hi = a.span_hi[r];
-                    if (hi > lo)
-                        bulk_load(st + a.f_off + ((size_t)lane * a.R + r) * a.S * 4u + lo * 8u,
-                                  a.freqs + p[r] * a.S + 2u * lo, (hi - lo) * 8u, &full[s]);
-                }
+            if (!fcont) {  // one copy per run of consecutive positions (always 1 with ids)
+                uint32_t n = 1;
+                while (lane + n < ntok && ((fstarts >> (lane + n)) & 1u) == 0u &&
+                       ((qok_mask >> (lane + n)) & 1u))
+                    ++n;
+                bulk_load(st + a.f_off + (size_t)lane * a.S * 4u, a.freqs + p * a.S, n * a.S * 4u,
+                          &full[s]);
             }
         }
     }
@@ -251,8 +231,8 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
             if (h_begin >= h_end) continue;
             // (cos, sin) of pairs 8m .. 8m+7
             float c[8], sn[8];
-            const float* frow = reinterpret_cast<const float*>(st + a.f_off) + (size_t)u * a.R * a.S;
-            if (a.mode != 2) {
+            const float* frow = reinterpret_cast<const float*>(st + a.f_off) + (size_t)u * a.S;
+            {
                 // The 8 lanes of a quarter-warp (m = 0..7) would read their
                 // float4 q at 64 m + 16 q: 2 bank groups, 4-way conflicts.
                 // Lane m reads them rotated by r = m / 2 (8 distinct bank
@@ -284,15 +264,6 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
                     sn[2 * q] = v.y;
                     c[2 * q + 1] = v.z;
                     sn[2 * q + 1] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t k = 8u * m + q;
-                    const float2 v =
-                        *reinterpret_cast<const float2*>(frow + (size_t)section_of(a, k) * a.S + 2u * k);
-                    c[q] = v.x;
-                    sn[q] = v.y;
                 }
             }
             const uint32_t e0 = INTERLEAVED ? 16u * m : 8u * m;
@@ -448,7 +419,7 @@ __device__ __forceinline__ void staged_prepare(const GqaArgs& a, const uint32_t*
                 bad = __ldg(a.position_ids + t) >= a.freqs_rows;
             } else {
                 for (uint32_t r = 0; r < 3; ++r)
-                    if (a.span_hi[r] > a.span_lo[r] &&
+                    if (section_used(a, r) &&
                         __ldg(a.position_ids + (uint64_t)r * a.T + t) >= a.freqs_rows)
                         bad = 1;
             }
@@ -691,21 +662,6 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     a.mode = position_ids ? (mrope_section ? 2u : 1u) : 0u;
     a.sec0 = sec0;
     a.sec01 = sec01;
-    if (a.mode == 2) {
-        // each mrope row only supplies its own section's pairs; copy that span
-        // widened to an even number of pairs (16-byte aligned, 16-byte sized)
-        const uint32_t lo[3] = {0u, sec0, sec01}, hi[3] = {sec0, sec01, S / 2};
-        a.R = 3;
-        for (int r = 0; r < 3; ++r) {
-            a.span_lo[r] = hi[r] > lo[r] ? (lo[r] & ~1u) : 0u;
-            a.span_hi[r] = hi[r] > lo[r] ? ((hi[r] + 1u) & ~1u) : 0u;
-        }
-    } else {
-        a.R = 1;
-        a.span_lo[0] = 0;
-        a.span_hi[0] = S / 2;
-        a.span_lo[1] = a.span_hi[1] = a.span_lo[2] = a.span_hi[2] = 0;
-    }
     a.items = (uint32_t)items;
     if (a.mode == 2) {
         const uint32_t threads = (uint32_t)((items + 31) / 32 * 32);
@@ -736,7 +692,7 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     // shared memory: barriers | ragged tables | kStages x (q | k | freqs | meta)
     const uint32_t tables = (uint32_t)(((2ull * num_batches + 1) * 4 + 127) / 128 * 128);
     const uint64_t per_tok = (uint64_t)num_q_heads * S * 2 + (uint64_t)a.Hk * S * esz +
-                             (uint64_t)a.R * S * 4 +
+                             (uint64_t)S * 4 +
                              sizeof(TokMeta);
     int dev = 0, optin = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -785,7 +741,7 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     a.q_off = 0;
     a.k_off = up16(tpb * num_q_heads * S * 2);
     a.f_off = a.k_off + up16(tpb * a.Hk * S * esz);
-    a.meta_off = a.f_off + up16(tpb * a.R * S * 4);
+    a.meta_off = a.f_off + up16(tpb * S * 4);
     a.stage_bytes = (uint32_t)((a.meta_off + tpb * sizeof(TokMeta) + 127) / 128 * 128);
     const uint32_t G = S / 16;
     a.slices = (uint32_t)(kConsumers / (tpb * G));
