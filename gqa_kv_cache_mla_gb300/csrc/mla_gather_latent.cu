@@ -135,8 +135,9 @@ __global__ void __launch_bounds__(kThreads, 4) gather_kernel(const GatherArgs a)
 }
 
 // Copy with dynamic per-row FP8.  A row's scale needs all of its 576 values,
-// so here a warp owns whole rows, kDynRows at a time (lane l holds pieces l,
-// l + 32 and, for l < 8, l + 64 of each): the row maxima are warp shuffles,
+// so here a warp owns whole rows, kDynRows at a time (lane l holds pieces l
+// and l + 32 of each, and the tail piece l % 8 of row l / 8): the row maxima
+// are integer maxima of bit patterns and one warp redux per row,
 // the scale and its reciprocal are computed in registers and every piece is
 // quantised from the registers that still hold it -- no shared-memory
 // reduction and no block barrier after the offsets are staged.  Warps are
@@ -152,6 +153,52 @@ __device__ __forceinline__ int64_t base_of(const int64_t (&base)[kDynRows], uint
 #pragma unroll
     for (uint32_t q = 1; q < kDynRows; ++q) b = i == q ? base[q] : b;
     return b;
+}
+
+// Bit pattern of the largest magnitude among 8 cache values, as an fp32
+// (non-negative floats order like their bit patterns).  bf16: the patterns
+// with the sign cleared order like the magnitudes, so a per-halfword
+// unsigned max finds it; E4M3 codes likewise per byte.  A NaN (a pattern
+// above infinity, or code 0x7F) falls back to the float maximum, which
+// ignores it, as the reference maximum does.
+template <bool CF8>
+__device__ __forceinline__ uint32_t piece_max_bits(const uint4& raw, float cache_scale) {
+    if (!CF8) {
+        const uint32_t acc = __vmaxu2(__vmaxu2(raw.x & 0x7fff7fffu, raw.y & 0x7fff7fffu),
+                                      __vmaxu2(raw.z & 0x7fff7fffu, raw.w & 0x7fff7fffu));
+        const uint32_t m = max(acc & 0xffffu, acc >> 16);
+        if (m <= 0x7f80u) return m << 16;
+    } else {
+        const uint32_t acc = __vmaxu4(raw.x & 0x7f7f7f7fu, raw.y & 0x7f7f7f7fu);
+        const uint32_t m = max(max(acc & 0xffu, (acc >> 8) & 0xffu), max((acc >> 16) & 0xffu, acc >> 24));
+        if (m != 0x7fu) {
+            const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(m), __NV_E4M3);
+            const float f = __half2float(__half(h));
+            return __float_as_uint(cache_scale == 1.0f ? f : __fmul_rn(f, cache_scale));
+        }
+    }
+    float v[8];
+    to_f32<CF8>(raw, cache_scale, v);
+    float f = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f = fmaxf(f, fabsf(v[e]));
+    return __float_as_uint(f);
+}
+
+// 8 cache values -> 8 E4M3 codes of value / sc (y = RN(1/sc); see div_refined).
+template <bool CF8>
+__device__ __forceinline__ uint2 quantize_piece(const uint4& raw, float cache_scale, float sc,
+                                                float y, bool fast) {
+    float v[8];
+    to_f32<CF8>(raw, cache_scale, v);
+    if (fast) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = div_refined(v[e], sc, y);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(v[e], sc);
+    }
+    return pack8_e4m3(v);
 }
 
 template <bool CF8>
@@ -176,71 +223,73 @@ __global__ void __launch_bounds__(kThreads, 3) gather_dynamic_kernel(const Gathe
     int64_t base_lane = (st < steps && lane < kDynRows) ? row_base(a, s_off, st * kDynRows + lane)
                                                          : -1;
     const bool bf16_values = !CF8 || a.cache_scale == 1.0f;
+    // lane l also moves the tail piece (columns 512 + 8 (l & 7) ..) of row
+    // l / 8, so every lane moves 9 pieces per step
+    const uint32_t tq = lane >> 3, tcol = 512u + 8u * (lane & 7u);
     for (; st < steps; st += nwarps) {
         int64_t base[kDynRows];
-        uint4 raw[kDynRows][3];
+        uint4 raw[kDynRows][2], rtail;
 #pragma unroll
         for (uint32_t q = 0; q < kDynRows; ++q) {
             base[q] = __shfl_sync(0xffffffffu, base_lane, q);
             if (base[q] >= 0) {
                 raw[q][0] = load_raw8<CF8>(a.cache, base[q] + lane * 8);
                 raw[q][1] = load_raw8<CF8>(a.cache, base[q] + 256 + lane * 8);
-                if (lane < 8) raw[q][2] = load_raw8<CF8>(a.cache, base[q] + 512 + lane * 8);
             }
         }
+        const int64_t btail = base_of(base, tq);
+        if (btail >= 0) rtail = load_raw8<CF8>(a.cache, btail + tcol);
         const uint32_t next = st + nwarps;
         base_lane = (next < steps && lane < kDynRows) ? row_base(a, s_off, next * kDynRows + lane)
                                                       : -1;
-        // row maxima: the kDynRows shuffle chains run side by side
-        float m[kDynRows];
+        // row maxima as bit patterns of non-negative floats (which order like
+        // the values): per lane, then one redux over the warp per row
+        uint32_t mtail = btail >= 0 ? piece_max_bits<CF8>(rtail, a.cache_scale) : 0u;
+        uint32_t mbits[kDynRows];
 #pragma unroll
         for (uint32_t q = 0; q < kDynRows; ++q) {
-            m[q] = 0.0f;
-            if (base[q] < 0) continue;
-#pragma unroll
-            for (uint32_t j = 0; j < 3; ++j) {
-                if (j == 2 && lane >= 8) break;
-                float v[8];
-                to_f32<CF8>(raw[q][j], a.cache_scale, v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m[q] = fmaxf(m[q], fabsf(v[e]));
+            uint32_t mq = tq == q ? mtail : 0u;
+            if (base[q] >= 0) {
+                mq = max(mq, piece_max_bits<CF8>(raw[q][0], a.cache_scale));
+                mq = max(mq, piece_max_bits<CF8>(raw[q][1], a.cache_scale));
             }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (uint32_t q = 0; q < kDynRows; ++q)
-                m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
+            mbits[q] = __reduce_max_sync(0xffffffffu, mq);
         }
         // lane q turns row q's maximum into its scale and reciprocal
-        float mine = m[0];
+        uint32_t mine = mbits[0];
 #pragma unroll
-        for (uint32_t q = 1; q < kDynRows; ++q) mine = lane == q ? m[q] : mine;
-        const float sc_lane = mine > 0.0f ? __fdiv_rn(mine, 448.0f) : 1.0f;
+        for (uint32_t q = 1; q < kDynRows; ++q) mine = lane == q ? mbits[q] : mine;
+        const float amax = __uint_as_float(mine);
+        const float sc_lane = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         const float y_lane = __frcp_rn(sc_lane);
         if (lane < kDynRows && base_of(base, lane) >= 0)
             scales[(uint64_t)st * kDynRows + lane] = sc_lane;
+        float sc[kDynRows], y[kDynRows];
 #pragma unroll
         for (uint32_t q = 0; q < kDynRows; ++q) {
-            const float sc = __shfl_sync(0xffffffffu, sc_lane, q);
-            const float y = __shfl_sync(0xffffffffu, y_lane, q);
+            sc[q] = __shfl_sync(0xffffffffu, sc_lane, q);
+            y[q] = __shfl_sync(0xffffffffu, y_lane, q);
+        }
+#pragma unroll
+        for (uint32_t q = 0; q < kDynRows; ++q) {
             if (base[q] < 0) continue;  // warp-uniform
             const uint64_t r = (uint64_t)st * kDynRows + q;
-            const bool fast = bf16_values && refined_ok(sc);
+            const bool fast = bf16_values && refined_ok(sc[q]);
 #pragma unroll
-            for (uint32_t j = 0; j < 3; ++j) {
-                if (j == 2 && lane >= 8) break;
-                float v[8];
-                to_f32<CF8>(raw[q][j], a.cache_scale, v);
-                if (fast) {
+            for (uint32_t j = 0; j < 2; ++j)
+                *reinterpret_cast<uint2*>(a.out + r * kRow + 256u * j + lane * 8) =
+                    quantize_piece<CF8>(raw[q][j], a.cache_scale, sc[q], y[q], fast);
+        }
+        if (btail >= 0) {
+            float st_ = sc[0], yt = y[0];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = div_refined(v[e], sc, y);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(v[e], sc);
-                }
-                *reinterpret_cast<uint2*>(a.out + r * kRow + 256u * j + lane * 8) = pack8_e4m3(v);
+            for (uint32_t q = 1; q < kDynRows; ++q) {
+                st_ = tq == q ? sc[q] : st_;
+                yt = tq == q ? y[q] : yt;
             }
+            const uint64_t r = (uint64_t)st * kDynRows + tq;
+            *reinterpret_cast<uint2*>(a.out + r * kRow + tcol) =
+                quantize_piece<CF8>(rtail, a.cache_scale, st_, yt, bf16_values && refined_ok(st_));
         }
     }
 }
