@@ -9,8 +9,9 @@
 // out per thread and iteration (grid-stride, 4 iterations in flight).  The
 // per-row quantiser gives each row to one warp.  Rows of up to 2048 values
 // are held in registers (one 16-byte load per lane and 256 columns, all
-// issued before any use), so the row is read from HBM once: warp
-// max-reduction of |x|, the scale, then the codes from the registers.  Longer
+// issued before any use), so the row is read from HBM once: max |x| as an
+// integer maximum of sign-cleared bf16 patterns and one warp redux, the
+// scale, then the codes from the registers.  Longer
 // rows take a two-pass loop (the second pass re-reads the row from L1/L2).
 //
 // The per-element division x / scale is the costly part of the quantiser
@@ -90,15 +91,28 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg_kernel(
 #pragma unroll
     for (int k = 0; k < VPL; ++k)
         v[k] = lane + 32u * k < nvec ? ld_stream(row + lane + 32u * k) : make_uint4(0, 0, 0, 0);
-    float amax = 0.0f;
+    // max |x| as the largest sign-cleared bf16 pattern (patterns order like
+    // magnitudes), a per-halfword unsigned max; a NaN (pattern above
+    // infinity) falls back to the float maximum, which ignores it
+    uint32_t acc = 0u;
 #pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-        float f[8];
-        unpack8(v[k], f);
+    for (int k = 0; k < VPL; ++k)
+        acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(v[k].x & 0x7fff7fffu, v[k].y & 0x7fff7fffu),
+                                     __vmaxu2(v[k].z & 0x7fff7fffu, v[k].w & 0x7fff7fffu)));
+    uint32_t mbits = max(acc & 0xffffu, acc >> 16);
+    if (mbits > 0x7f80u) {
+        float amax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        for (int k = 0; k < VPL; ++k) {
+            float f[8];
+            unpack8(v[k], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        }
+        mbits = __float_as_uint(amax) >> 16;
     }
-    const float sc = row_scale(amax);
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, mbits) << 16);
+    const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     if (lane == 0) scales[r] = sc;
     uint2* orow = reinterpret_cast<uint2*>(out + (int64_t)r * out_stride);
     if (refined_ok(sc)) {
