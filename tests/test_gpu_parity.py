@@ -700,6 +700,18 @@ def test_quantize_rows_long_and_strided(orc, dev, rows, cols, in_stride, out_str
     assert np.array_equal(got[:, cols:], out0[:, cols:])  # the row padding is not written
 
 
+def test_convert_benchmark_shape(orc, dev):
+    """The 2^26-value launch the benchmark times, every code compared."""
+    import torch
+
+    w = W.fp8_convert()
+    d = dev.DeviceConvert(w)
+    d.run()
+    torch.cuda.synchronize()
+    assert d.guards_intact()
+    assert np.array_equal(d.out.host(), orc.convert_bf16_to_e4m3(w.x, w.scale))
+
+
 def test_quantize_rows_benchmark_shape(orc, dev):
     import torch
 
