@@ -221,3 +221,23 @@ def test_gather_dynamic_host_checks():
     assert f(FAKE, FAKE, None, 1, FAKE, 2, 8, None, 0) == kvw.KVW_EINVAL
     c2 = _mla_cache(head_size=512)
     assert f(FAKE, FAKE, ctypes.byref(c2), 1, FAKE, 2, 8, None, 0) == kvw.KVW_EUNSUPPORTED
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library the binding raises: there is no fallback path
+    that could compute anything elsewhere."""
+    monkeypatch.setattr(kvw, "LIB_PATH", str(tmp_path / "libkvw.so"))
+    with pytest.raises(ImportError, match="library missing"):
+        kvw._load()
+
+
+def test_product_package_does_not_import_the_oracle():
+    """The package (binding, device helpers, generators, profiling driver)
+    never imports the CPU reference: only tests and the benchmark's baseline
+    leg may."""
+    import pathlib
+
+    pkg = pathlib.Path(kvw.__file__).parent
+    for f in pkg.glob("*.py"):
+        text = f.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, f.name
