@@ -1,10 +1,16 @@
 /*
  * kvw.h - C ABI of the GB300 fused per-token KV-cache write library.
  *
- * Three entry points, one per operation of the Modular MAX kernel pages:
- *   kvw_mla_rope_rmsnorm_quant   "mla_fused_rope_rmsnorm_quantization"
- *   kvw_qk_rope_paged_ragged     "generic_fused_qk_rope_bshd_paged_ragged"
- *   kvw_rms_norm_kv_cache_paged  "rms_norm_kv_cache_ragged_paged"
+ * One entry point per operation of the Modular MAX kernel pages:
+ *   kvw_mla_rope_rmsnorm_quant         "mla_fused_rope_rmsnorm_quantization"
+ *   kvw_qk_rope_paged_ragged           "generic_fused_qk_rope_bshd_paged_ragged"
+ *   kvw_rms_norm_kv_cache_paged        "rms_norm_kv_cache_ragged_paged"
+ * and for the steps of the "mla_graph" module page around them:
+ *   kvw_mla_rope_rmsnorm_inplace       fused_rope_rmsnorm_kernel
+ *   kvw_mla_gather_latent              mla_prefill_branch_fp8 (latent copy)
+ *   kvw_mla_gather_latent_fp8_dynamic  the same with dynamic FP8 scaling
+ *   kvw_convert_bf16_to_fp8_e4m3       convert_bf16_to_fp8_e4m3fn
+ *   kvw_quantize_fp8_rows              dynamic FP8 scaling, one scale per row
  *
  * Conventions shared by every call
  * --------------------------------
@@ -48,6 +54,11 @@
  *   (KVW_EINVAL otherwise).
  * - Aliasing: rows of different tokens must map to different cache slots
  *   (page tables hold distinct pages); otherwise the result is undefined.
+ * - Size limits (KVW_EUNSUPPORTED beyond them): num_batches <= 8192; MLA
+ *   tot_seq_len * num_heads * 8 <= 0xFFFFF000 (16-byte q vectors); GQA
+ *   head_size a multiple of 16 and <= 512, and (num_q_heads + num_heads) *
+ *   head_size / 16 <= 1024; K-norm gamma_len <= 2048 and normalised rows
+ *   (tokens x heads) <= 0xFFFFF000.
  */
 #ifndef KVW_H
 #define KVW_H
