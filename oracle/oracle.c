@@ -2,7 +2,7 @@
  * CPU oracle for the fused per-token KV-cache write path.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
- * statement of what the three entry points compute.  Only the test suite,
+ * statement of what the library's entry points compute.  Only the test suite,
  * the package smoke check and the benchmark's CPU-baseline leg load it; the
  * CUDA library never calls, links or includes it, and it shares no code,
  * header, table or helper with the CUDA sources.
@@ -17,8 +17,11 @@
  *    the three fused operations; Args q_rope_output, q_rope,
  *    input_row_offsets, freqs_cis, gamma, kv_collection, layer_idx, epsilon;
  *    Parameters kv_input_fn.
- *  - "mla_graph" (Mojo module): Functions list, entry
- *    fused_rope_rmsnorm_quantization_kernel (quantise before the cache write).
+ *  - "mla_graph" (Mojo module): module description (dynamic FP8 scaling);
+ *    Functions list, entries fused_rope_rmsnorm_quantization_kernel (quantise
+ *    before the cache write), fused_rope_rmsnorm_kernel (the in-place
+ *    variant), mla_prefill_branch_fp8 (copy the latent values out of the
+ *    paged cache, then quantise them) and convert_bf16_to_fp8_e4m3fn.
  *  - "generic_fused_qk_rope_bshd_paged_ragged" (Mojo function): description
  *    (Q rotated into output, K rotated in the paged cache); Parameters
  *    interleaved, has_position_ids, mrope_section; Args q_proj,
