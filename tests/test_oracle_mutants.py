@@ -61,6 +61,11 @@ MUTANTS = [
      "float a = oracle_bf16_to_f32(in[r * in_stride + c]);"),
     ("gather position off by one", "uint64_t pos = r - ctx_offsets[b];",
      "uint64_t pos = r - ctx_offsets[b] + 1;"),
+    ("whole-row norm over the first head only",
+     "rms_norm_bf16((const uint16_t* const*)ptrs, ptrs, (int64_t)num_kv_heads * head_size, w,",
+     "rms_norm_bf16((const uint16_t* const*)ptrs, ptrs, (int64_t)head_size, w,"),
+    ("cast-first norm without the intermediate rounding",
+     "float xr_c = oracle_bf16_to_f32(oracle_f32_to_bf16(xr));", "float xr_c = xr;"),
     ("dynamic gather ignores the cache scale",
      "v[j] = load_elem(cache, base + j, cache_dtype, cache_scale);",
      "v[j] = load_elem(cache, base + j, cache_dtype, 1.0f);"),
@@ -88,6 +93,8 @@ PINS = [
     (N.test_mla_latent_part_vs_torch, {}),
     (N.test_knorm_subset_vs_torch, {"G": 16}),
     (N.test_knorm_weight_offset_adds_to_gamma, {}),
+    (N.test_knorm_whole_row_norm, {}),
+    (N.test_knorm_multiply_after_cast_within_one_ulp, {}),
     (S.test_mla_tiny_writes_exactly_new_rows, {"dtype": 1}),
     (S.test_gqa_rotates_only_new_k_rows, {}),
     (S.test_knorm_touches_only_leading_cols_of_new_rows, {}),
