@@ -47,10 +47,11 @@
  *    position from row sec(k) of position_ids[3][T].
  *  - FP8 cache values are stored as satfinite_rne(y / scale).
  *  - multiply_before_cast=false rounds the normalised value to the cache
- *    type first and then multiplies by the weight (parity unpinned).
+ *    type first and then multiplies by the weight (a reading the pages do
+ *    not fix; pinned by its power-of-two-weight special case).
  *  - per_head_norm=false normalises the whole K row of a token
- *    (num_heads * head_size values) with a gamma of that length (parity
- *    unpinned).
+ *    (num_heads * head_size values) with a gamma of that length (a reading
+ *    the pages do not fix; pinned against a float64 library norm).
  *
  * Error flags (returned, OR of):
  *   1 = a slot maps to no valid page (page index past the table, or a page

@@ -138,3 +138,17 @@ def test_knorm_whole_row_norm(orc):
         ref_bits = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(
             np.uint16)
         assert bf16_ulp_diff(after[page, 0, w.layer_idx, row].reshape(-1), ref_bits).max() <= 1
+
+
+@pytest.mark.parametrize("gamma_value,wo", [(1.0, 0.0), (2.0, 0.0), (0.25, 0.75), (0.5, -0.25)])
+def test_knorm_cast_first_reduces_to_one_rounding_for_power_of_two_weights(orc, gamma_value, wo):
+    """multiply_before_cast=False rounds x*r to bf16 and then multiplies by
+    w = gamma + weight_offset; when w is a power of two that product is exact,
+    so the two orders give the same bits."""
+    a = _knorm_small(32, mbc=True, wo=wo)
+    b = _knorm_small(32, mbc=False, wo=wo)
+    for w in (a, b):
+        w.gamma = np.full_like(w.gamma, W.bf16_bits(np.float32(gamma_value)))
+    ca, _ = orc.rms_norm_kv_cache_paged(a)
+    cb, _ = orc.rms_norm_kv_cache_paged(b)
+    assert np.array_equal(ca, cb)
