@@ -210,10 +210,3 @@ def for_workload(w, device="cuda", guard=True):
     cls = {W.MLAWorkload: DeviceMLA, W.GQAWorkload: DeviceGQA, W.KNormWorkload: DeviceKNorm,
            W.GatherWorkload: DeviceGather, W.ConvertWorkload: DeviceConvert}[type(w)]
     return cls(w, device=device, guard=guard)
-
-
-def for_workload(w, device="cuda", guard=True):
-    """The Device* holder matching the type of workload ``w``."""
-    cls = {W.MLAWorkload: DeviceMLA, W.GQAWorkload: DeviceGQA, W.KNormWorkload: DeviceKNorm,
-           W.GatherWorkload: DeviceGather, W.ConvertWorkload: DeviceConvert}[type(w)]
-    return cls(w, device=device, guard=guard)

@@ -3,8 +3,9 @@
  * cache write on a small ragged batch (2 requests, new tokens [3, 5], prior
  * lengths [0, 7], 4 q heads, page size 16, layer 1 of 2), copy the results
  * back and compare them with the CPU reference on the same inputs: query
- * rows within 1 bf16 ulp, written cache rows within 1 ulp of the cache
- * type, every other cache byte unchanged, equal error flags.
+ * rows within 1 bf16 ulp, written cache rows within 1 bf16 ulp (bf16 cache)
+ * or 1 E4M3 ulp on at most 0.1% of the written values (FP8 cache), every
+ * other cache byte unchanged, equal error flags.
  *
  * Usage: abi_mla <cache dtype: 0 bf16 | 1 fp8>   (exit status 0 on success)
  */
@@ -139,6 +140,7 @@ int main(int argc, char** argv) {
                                  (int64_t)(pos % P) * s_token;
             memset(written + base, 1, ROW);
         }
+    size_t n_written = 0, n_fp8_off = 0;
     for (size_t i = 0; i < n_cache; ++i) {
         int d;
         if (fp8)
@@ -150,6 +152,13 @@ int main(int argc, char** argv) {
             d = abs(bf16_ordinal(a) - bf16_ordinal(r));
         }
         if (d > (written[i] ? 1 : 0)) ++bad;
+        n_written += written[i];
+        if (fp8 && written[i] && d == 1) ++n_fp8_off;
+    }
+    /* FP8: 1-ulp differences allowed on at most 0.1% of the written values */
+    if (fp8 && (double)n_fp8_off > 1e-3 * (double)n_written) {
+        fprintf(stderr, "fp8: %zu of %zu written values 1 ulp off\n", n_fp8_off, n_written);
+        ++bad;
     }
     printf("kvw %d (%s cache): %d mismatches, flags %u\n", kvw_version(), fp8 ? "fp8" : "bf16",
            bad, f_gpu);
