@@ -1,13 +1,15 @@
 #!/usr/bin/env python3
 """Benchmark of the fused per-token KV-cache write on GB300.
 
-Default workload: MLA decode, DeepSeek-V3 shape (256 requests x 1 new token,
-prior lengths U[1,8192], 128 q heads, 512 latent + 64 rope, page 128, FP8
-E4M3 cache out with scale 1.0).  A step is one call of
-``kvw_mla_rope_rmsnorm_quant`` over that batch: RoPE on q_rope and on the
-rope part, RMSNorm of the latent part, FP8 quantisation and the paged
-scatter.  Other workloads (``--workload``) measure the prefill, GQA and
-K-norm launches the same way.
+Default workload: MLA ragged prefill (16 requests, new lengths U[512,8192],
+70,820 tokens with the benchmark seed, 128 q heads, 512 latent + 64 rope,
+page 128, FP8 E4M3 cache out with scale 1.0), the largest configuration of
+the MLA write.  A step is one call of ``kvw_mla_rope_rmsnorm_quant`` over that
+batch: RoPE on q_rope and on the rope part, RMSNorm of the latent part, FP8
+quantisation and the paged scatter.  The same run then measures, under the
+line's ``also`` key, the MLA decode step (256 requests x 1 token, with its
+end-to-end figure), the bf16-cache prefill, the GQA Q/K RoPE and the K-cache
+RMSNorm launches the same way.  ``--workload`` picks another main workload.
 
 Timing: W warm-up steps, then K timed steps between a barrier and a device
 synchronize on both sides.  Each step's launch is bracketed by CUDA events on
@@ -45,6 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 WORKLOADS = W.REGISTRY
 DEFAULT_SEED = 2
+DEFAULT_WORKLOAD = "mla_prefill_fp8"
+# measured after the main workload, in the same run, under the line's "also" key
+DEFAULT_ALSO = ("mla_decode", "mla_prefill_bf16", "gqa_interleaved", "knorm128", "knorm64")
+HEADLINE = ("mla_prefill_fp8", "mla_prefill_bf16", "mla_decode", "mla_decode_bf16")
 
 
 def kind_of(w):
@@ -267,6 +273,28 @@ def cpu_baseline(w, name, budget_s, single_thread=True):
     return res
 
 
+def unit_of(w):
+    return "tokens/s" if kind_of(w) in ("mla", "gqa", "kno") else "rows/s"
+
+
+def metric_of(name, unit):
+    return METRIC if name in HEADLINE else "%s %s; achieved HBM GB/s vs peak" % (name, unit)
+
+
+def config_of(name, w, world):
+    """The workload description both arms print (identical keys and values)."""
+    abytes = algorithmic_bytes(w, name)
+    k = kind_of(w)
+    fp8_out = (getattr(getattr(w, "cache", None), "dtype", 0) == W.DTYPE_FP8_E4M3
+               or k == "codec" or (k == "gather" and w.out_dtype == W.DTYPE_FP8_E4M3))
+    return {"workload": name + ": " + WORKLOADS[name][2], "tokens_per_gpu": int(w.T),
+            "l2": ("flushed before every GPU step (512 MiB written, 512 MiB read)"
+                   if abytes < 2 * L2_BYTES else
+                   "inputs larger than L2 (%.2f GB per step)" % (abytes / 1e9)),
+            "io": "bf16 in, fp32 arithmetic, %s out" % ("e4m3" if fp8_out else "bf16"),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -287,15 +315,14 @@ def run_reference(args):
             times.append(w.T / cb["value"])
     ms = 1000.0 * statistics.mean(times)
     value = w.T / (ms / 1000.0)
-    unit = "tokens/s" if kind_of(w) in ("mla", "gqa", "kno") else "rows/s"
+    unit = unit_of(w)
     line = {"impl": "reference",
-            "metric": METRIC if name == "mla_decode" else "%s %s; achieved HBM GB/s vs peak" % (
-                name, unit),
+            "metric": metric_of(name, unit),
             "value": value, "unit": unit,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": name + ": " + WORKLOADS[name][2], "tokens": w.T},
+            "data": "synthetic (seeded; shapes and distributions of the benchmark configs)",
+            "config": config_of(name, w, world),
             "cpu_baseline": {"value": value, "unit": unit, "cores": threads,
                              "kind": "oracle",
                              "sample": "each step: whole %d-token batches for %.2f s" %
@@ -306,20 +333,29 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+class Flusher:
+    """Evicts the L2 between timed steps: 512 MiB written, then 512 MiB read."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.fw = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.fr = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.fw.fill_(1)
+        self.fr.sum()
+
+
+def measure(name, steps, warmup, dev, rank, world, flusher, e2e=True, cpu_s=None):
+    """Device-timed throughput of one workload (and optionally its end-to-end
+    figure and the oracle beside it).  Returns the fields of a bench line."""
     import torch
     import torch.distributed as dist
 
-    rank, local_rank, world = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
     from gqa_kv_cache_mla_gb300 import device as D
-    from gqa_kv_cache_mla_gb300 import kvw
 
-    name = args.workload
-    builder, kfile, desc = WORKLOADS[name]
+    builder, kfile, _ = WORKLOADS[name]
     # replicas: each rank writes its own independent batch (weak scaling)
     w = builder(DEFAULT_SEED + 100 * rank)
     k = kind_of(w)
@@ -329,34 +365,26 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     run = lambda: d.run(stream=stream)
     abytes = algorithmic_bytes(w, name)
-    footprint = abytes
-    flush = footprint < 2 * L2_BYTES
-    if flush:
-        fw = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-        fr = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    flush = abytes < 2 * L2_BYTES
 
-    def l2_flush():
-        fw.fill_(1)
-        fr.sum()
-
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         if flush:
-            l2_flush()
+            flusher()
         run()
     torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
+          for _ in range(steps)]
+    clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         if flush:
-            l2_flush()
+            flusher()
         ev[i][0].record(stream)
         run()
         ev[i][1].record(stream)
@@ -368,62 +396,197 @@ def run_ours(args):
     per = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(per)
     ms_max, tokens_all = combine_ranks(ms, w.T, world, dev)
-    value = tokens_all / (ms_max / 1000.0)
-    unit = "tokens/s" if k in ("mla", "gqa", "kno") else "rows/s"
+    unit = unit_of(w)
     assert d.flags() == 0, "kernel reported data errors on the benchmark inputs"
     if k == "mla" and w.inplace:  # restore the rows the in-place steps rewrote
         d.cache.reset(w.cache.data)
 
     # end to end through the public API: pinned host inputs -> device, launch,
     # q/output and the error word back to the host, every step
-    e2e = None
-    if not args.no_e2e and k in ("mla", "gqa", "kno") and not getattr(w, "inplace", False):
-        e2e = measure_e2e(d, w, k, stream, dev, max(3, min(args.steps, 200)), args.warmup)
-        e2e["ms"], _ = combine_ranks(e2e["ms"], w.T, world, dev)
-        e2e = {"value": tokens_all / (e2e["ms"] / 1000.0), "unit": "tokens/s",
-               "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-               "ms_per_step": e2e["ms"],
-               "how": "every step: one copy of its packed inputs (and a zeroed error word) "
-                      "from pinned host memory, the kvw call, one copy of the error word and "
-                      "the outputs back to pinned host memory; steps pipelined %d deep on "
-                      "copy-in / compute / copy-out streams, %d steps per CUDA graph replay" % (
-                          e2e["depth"], e2e["per_graph"])}
+    e2e_line = None
+    if e2e and k in ("mla", "gqa", "kno") and not getattr(w, "inplace", False):
+        r = measure_e2e(d, w, k, stream, dev, max(3, min(steps, 200)), warmup)
+        r["ms"], _ = combine_ranks(r["ms"], w.T, world, dev)
+        floor = copy_floor(r["h2d"], r["d2h"], dev, reps=max(8, min(steps, 64)))
+        e2e_line = {"value": tokens_all / (r["ms"] / 1000.0), "unit": unit,
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                    "ms_per_step": r["ms"],
+                    "copy_floor_ms": floor["both_ms"], "e2e_over_copy_floor":
+                        r["ms"] / floor["both_ms"] if floor["both_ms"] else None,
+                    "copy_floor": floor,
+                    "how": "every step: one copy of its packed inputs (and a zeroed error "
+                           "word) from pinned host memory, the kvw call, one copy of the "
+                           "error word and the outputs back to pinned host memory; steps "
+                           "pipelined %d deep on copy-in / compute / copy-out streams, %d "
+                           "steps per CUDA graph replay" % (r["depth"], r["per_graph"])}
 
     peak, peak_src = measured_peak()
     achieved = abytes / (ms / 1000.0) / 1e9
-    traffic = ncu_traffic(name, kfile)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": abytes,
-            "peak_source": peak_src, "kernel": kfile.replace(".cu", "")}
-
+            "frac": achieved / peak, "traffic": ncu_traffic(name, kfile),
+            "algorithmic_bytes": abytes, "peak_source": peak_src,
+            "kernel": kfile.replace(".cu", "")}
+    host_us = host_call_us(run, stream) if name in ("mla_decode",) else None
+    if k == "mla" and w.inplace:
+        d.cache.reset(w.cache.data)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, name, budget_s=args.cpu_s)
+    if cpu_s and rank == 0 and world == 1:
+        cpu = cpu_baseline(w, name, budget_s=cpu_s)
+    out = {"name": name, "value": tokens_all / (ms_max / 1000.0), "unit": unit,
+           "ms_per_step": ms_max, "steps": steps, "config": config_of(name, w, world),
+           "roofline": roof, "e2e": e2e_line, "cpu_baseline": cpu, "clocks": clk,
+           "timing": {"ms_median": statistics.median(per), "ms_min": min(per),
+                      "wall_s_timed_region": wall,
+                      "kernel_source_sha256_16": source_hash(kfile)},
+           "host_us_per_call": host_us}
+    del d
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from gqa_kv_cache_mla_gb300 import kvw  # noqa: F401  (fails loudly without the library)
+
+    flusher = Flusher(dev)
+    main_r = measure(args.workload, args.steps, args.warmup, dev, rank, world, flusher,
+                     e2e=not args.no_e2e, cpu_s=None if args.no_cpu_baseline else args.cpu_s)
+    also = []
+    for name in args.also:
+        if name == args.workload:
+            continue
+        steps = args.also_steps or default_steps(name)
+        r = measure(name, steps, args.warmup, dev, rank, world, flusher,
+                    e2e=not args.no_e2e and name in ("mla_decode",), cpu_s=None)
+        also.append({"workload": r["config"]["workload"], "value": r["value"],
+                     "unit": r["unit"], "ms_per_step": r["ms_per_step"], "steps": steps,
+                     "roofline": {x: r["roofline"][x] for x in
+                                  ("achieved", "frac", "algorithmic_bytes", "traffic",
+                                   "kernel")},
+                     "e2e": r["e2e"], "clocks": r["clocks"],
+                     "host_us_per_call": r["host_us_per_call"],
+                     "ms_median": r["timing"]["ms_median"], "ms_min": r["timing"]["ms_min"]})
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return 0
     line = {
-        "metric": (METRIC if name == "mla_decode" else
-                   "%s %s; achieved HBM GB/s vs peak" % (name, unit)),
-        "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "metric": metric_of(args.workload, main_r["unit"]),
+        "value": main_r["value"], "unit": main_r["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes and distributions of the benchmark configs)",
-        "config": {"workload": name + ": " + desc, "tokens_per_gpu": w.T,
-                   "l2": ("flushed before every step (512 MiB written, 512 MiB read)" if flush
-                          else "inputs larger than L2 (%.2f GB per step)" % (abytes / 1e9)),
-                   "io": "bf16 in, fp32 arithmetic, %s out" %
-                         ("e4m3" if (getattr(getattr(w, "cache", None), "dtype", 0) ==
-                                     W.DTYPE_FP8_E4M3 or k == "codec") else "bf16"),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
-        "clocks": clk,
-        "timing": {"ms_median": statistics.median(per), "ms_min": min(per),
-                   "wall_s_timed_region": wall, "kernel_source_sha256_16": source_hash(kfile)},
+        "config": main_r["config"],
+        "roofline": main_r["roofline"], "cpu_baseline": main_r["cpu_baseline"],
+        "e2e": main_r["e2e"], "gpu_launches": args.steps, "clocks": main_r["clocks"],
+        "timing": main_r["timing"],
+        "also": also,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def copy_floor(h2d, d2h, dev, reps=32):
+    """Plain pinned copies of one e2e step's byte counts (one cudaMemcpyAsync
+    each way per step): host->device alone, device->host alone, and both at
+    once on two streams (the floor for a step whose copies overlap)."""
+    import torch
+
+    h_src = torch.empty(max(h2d, 16), dtype=torch.uint8, pin_memory=True)
+    d_dst = torch.empty(max(h2d, 16), dtype=torch.uint8, device=dev)
+    d_src = torch.zeros(max(d2h, 16), dtype=torch.uint8, device=dev)
+    h_dst = torch.empty(max(d2h, 16), dtype=torch.uint8, pin_memory=True)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    launch = torch.cuda.current_stream(dev)
+
+    def timed(do_in, do_out):
+        for n in range(reps + 2):  # 2 untimed, then reps timed
+            if n == 2:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(launch)
+                s_in.wait_stream(launch)
+                s_out.wait_stream(launch)
+            if do_in:
+                with torch.cuda.stream(s_in):
+                    d_dst[:h2d].copy_(h_src[:h2d], non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(s_out):
+                    h_dst[:d2h].copy_(d_src[:d2h], non_blocking=True)
+        launch.wait_stream(s_in)
+        launch.wait_stream(s_out)
+        b.record(launch)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    r = {"h2d_ms": timed(True, False) if h2d else 0.0,
+         "d2h_ms": timed(False, True) if d2h else 0.0}
+    r["both_ms"] = timed(h2d > 0, d2h > 0) if (h2d or d2h) else 0.0
+    r["h2d_gbs"] = h2d / (r["h2d_ms"] / 1e3) / 1e9 if r["h2d_ms"] else None
+    r["d2h_gbs"] = d2h / (r["d2h_ms"] / 1e3) / 1e9 if r["d2h_ms"] else None
+    r["numa"] = numa_info(dev)
+    return r
+
+
+def numa_info(dev):
+    """NUMA node of the GPU's PCI device and the nodes of this process's CPUs
+    (pinned buffers are placed on the allocating CPU's node)."""
+    out = {"gpu_node": None, "cpu_nodes": None}
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(dev.index), "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True,
+                             timeout=20).stdout.strip().lower()
+        dom, rest = bus.split(":", 1)
+        path = "/sys/bus/pci/devices/%s:%s/numa_node" % (dom[-4:], rest)
+        out["gpu_node"] = int(open(path).read().strip())
+    except Exception:
+        pass
+    try:
+        cpus = os.sched_getaffinity(0)
+        nodes = set()
+        base = "/sys/devices/system/node"
+        for nd in os.listdir(base):
+            if not re.fullmatch(r"node\d+", nd):
+                continue
+            spec = open(os.path.join(base, nd, "cpulist")).read().strip()
+            ids = set()
+            for part in filter(None, spec.split(",")):
+                lo, _, hi = part.partition("-")
+                ids.update(range(int(lo), int(hi or lo) + 1))
+            if ids & cpus:
+                nodes.add(int(nd[4:]))
+        out["cpu_nodes"] = sorted(nodes)
+    except Exception:
+        pass
+    return out
+
+
+def host_call_us(run, stream, calls=1000):
+    """Host time of one entry-point call (argument checks, device queries,
+    launch), measured while the stream is held busy by a bounded sleep
+    kernel so the calls only queue: wall time of ``calls`` calls / calls."""
+    import torch
+
+    run()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000_000)  # about 0.1 s at 2 GHz
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        run()
+    el = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    return el / calls * 1e6
+
+
+def default_steps(name):
+    return {"mla_decode": 4000, "mla_decode_bf16": 4000}.get(name, 300)
 
 
 def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=3, per_graph=32, chunks=1):
@@ -584,11 +747,18 @@ def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=3, per_graph=32, chun
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of the job: 1, or the torchrun world size (one rank per GPU)")
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mla_decode")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--also", default=None,
+                    help="comma-separated workloads measured after the main one ('' for none; "
+                         "default: %s with the default workload, none otherwise)" %
+                         ",".join(DEFAULT_ALSO))
+    ap.add_argument("--also-steps", type=int, default=None,
+                    help="timed steps of each 'also' workload (default: its own count)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-s", type=float, default=10.0,
@@ -598,8 +768,19 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    world = dist_env()[2]
+    if args.gpus != world:
+        ap.error("--gpus %d but WORLD_SIZE is %d: launch N > 1 GPUs with torchrun "
+                 "(--nproc-per-node N), one rank per GPU" % (args.gpus, world))
+    if args.also is None:
+        args.also = list(DEFAULT_ALSO) if args.workload == DEFAULT_WORKLOAD else []
+    else:
+        args.also = [x for x in args.also.split(",") if x]
+        bad = [x for x in args.also if x not in WORKLOADS]
+        if bad:
+            ap.error("unknown workloads: %s" % ",".join(bad))
     if args.steps is None:
-        args.steps = {"mla_decode": 4000, "mla_decode_bf16": 4000}.get(args.workload, 300)
+        args.steps = default_steps(args.workload)
         if args.impl == "reference":
             args.steps = 5
     if args.impl == "reference":

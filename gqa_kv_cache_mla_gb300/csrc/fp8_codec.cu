@@ -169,10 +169,8 @@ extern "C" int kvw_convert_bf16_to_fp8_e4m3(void* out, const void* in, uint64_t 
         (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
         return KVW_EINVAL;
     if (!(scale > 0.0f && scale < 3.0e38f)) return KVW_EINVAL;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return KVW_ECUDA;
+    int sms = 0;
+    if (sm_count(sms) != cudaSuccess) return KVW_ECUDA;
     const uint64_t nvec = n / 8;
     uint64_t blocks = (nvec + kThreads - 1) / kThreads;
     const uint64_t cap = (uint64_t)sms * 8;  // 8 resident CTAs per SM, grid-stride beyond

@@ -7,6 +7,7 @@
 // request -> slot position) that every kernel starts with.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -325,5 +326,87 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// ------------------------------------------------------------ host: launch facts
+
+// The launchers run on every call of a serving loop, where a driver query per
+// call would cost about as much as a decode kernel.  The facts below are
+// queried once per device (occupancy once per kernel instance, device and
+// launch shape) and kept for the life of the process; the cached words are
+// read and written atomically, so concurrent callers at worst repeat a query.
+constexpr int kMaxDevices = 64;
+
+// Attribute ATTR of the current device.
+template <int ATTR>
+inline cudaError_t device_attr(int& out) {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (cacheable) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) {
+            out = v;
+            return cudaSuccess;
+        }
+    }
+    e = cudaDeviceGetAttribute(&out, static_cast<cudaDeviceAttr>(ATTR), dev);
+    if (e == cudaSuccess && cacheable && out > 0) cache[dev].store(out, std::memory_order_relaxed);
+    return e;
+}
+
+inline cudaError_t sm_count(int& out) { return device_attr<cudaDevAttrMultiProcessorCount>(out); }
+inline cudaError_t smem_optin(int& out) {
+    return device_attr<cudaDevAttrMaxSharedMemoryPerBlockOptin>(out);
+}
+
+// Allow kernel K `smem` bytes of dynamic shared memory on the current device
+// (the attribute is raised once per device to the largest size asked for).
+template <auto K>
+inline cudaError_t prepare_smem(size_t smem) {
+    static std::atomic<uint64_t> allowed[kMaxDevices];
+    if (smem == 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (cacheable && allowed[dev].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess || !cacheable) return e;
+    uint64_t prev = allowed[dev].load(std::memory_order_relaxed);
+    while (prev < smem && !allowed[dev].compare_exchange_weak(prev, smem)) {
+    }
+    return cudaSuccess;
+}
+
+// CTAs of kernel K resident on the whole current device at once with
+// `threads` threads and `smem` bytes of dynamic shared memory (0 when none
+// fits); also allows K that much shared memory.
+template <auto K>
+inline cudaError_t wave_ctas(int threads, size_t smem, uint64_t& out) {
+    static std::atomic<uint64_t> occ[kMaxDevices];  // smem << 24 | threads << 8 | per SM
+    cudaError_t e = prepare_smem<K>(smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = sm_count(sms)) != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    const uint64_t key = ((uint64_t)smem << 24) | ((uint64_t)threads << 8);
+    if (cacheable) {
+        const uint64_t v = occ[dev].load(std::memory_order_relaxed);
+        if ((v & ~0xffull) == key && (v & 0xffull) != 0) {
+            out = (uint64_t)sms * (v & 0xffull);
+            return cudaSuccess;
+        }
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, K, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (cacheable && per_sm > 0 && per_sm < 256)
+        occ[dev].store(key | (uint64_t)per_sm, std::memory_order_relaxed);
+    out = (uint64_t)sms * (uint64_t)(per_sm > 0 ? per_sm : 0);
+    return cudaSuccess;
+}
 
 }  // namespace kvw

@@ -296,39 +296,27 @@ __global__ void __launch_bounds__(kThreads, 3) gather_dynamic_kernel(const Gathe
 
 template <bool CF8, bool OF8>
 cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
-    auto k = gather_kernel<CF8, OF8>;
+    constexpr auto k = gather_kernel<CF8, OF8>;
     const size_t smem = sizeof(uint32_t) * ((size_t)a.B + 1);
-    if (smem > 32 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    uint64_t wave = 0;
+    const cudaError_t e = wave_ctas<k>(kThreads, smem, wave);
     if (e != cudaSuccess) return e;
+    if (wave == 0) return cudaErrorInvalidConfiguration;
     const uint32_t tiles = (a.rows + kTileRows - 1) / kTileRows;
-    const uint32_t wave = (uint32_t)(sms * (per_sm > 0 ? per_sm : 1));
-    k<<<tiles < wave ? tiles : wave, kThreads, smem, stream>>>(a);
+    k<<<tiles < wave ? tiles : (uint32_t)wave, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <bool CF8>
 cudaError_t launch_dynamic(const GatherArgs& a, float* scales, cudaStream_t stream) {
-    auto k = gather_dynamic_kernel<CF8>;
+    constexpr auto k = gather_dynamic_kernel<CF8>;
     const size_t smem = sizeof(uint32_t) * ((size_t)a.B + 1);
-    if (smem > 32 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    uint64_t wave = 0;
+    const cudaError_t e = wave_ctas<k>(kThreads, smem, wave);
     if (e != cudaSuccess) return e;
+    if (wave == 0) return cudaErrorInvalidConfiguration;
     const uint32_t ctas = (a.rows + kDynRows * (kThreads / 32) - 1) / (kDynRows * (kThreads / 32));
-    const uint32_t wave = (uint32_t)(sms * (per_sm > 0 ? per_sm : 1));
-    k<<<ctas < wave ? ctas : wave, kThreads, smem, stream>>>(a, scales);
+    k<<<ctas < wave ? ctas : (uint32_t)wave, kThreads, smem, stream>>>(a, scales);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,14 @@
 //   * every CTA stages input_row_offsets and cache_lengths in shared memory,
 //     validates them and binary-searches its tokens' requests there.
 // Both roles live in one launch so a decode step is one kernel.
+// Decode fast path: when the batch has as many tokens as requests, the
+// offsets are most likely the identity (one new token per request), so
+// token t is request t at slot position cache_lengths[t].  A CTA then loads
+// cache_lengths first, issues the dependent page-table and freqs loads
+// straight from registers (no staging, search or barrier in between), and
+// checks the identity over the whole offsets table with one block vote taken
+// while those loads are in flight; a CTA that finds anything else runs the
+// general path above, so results and flags are the same either way.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -51,6 +59,7 @@ struct MlaArgs {
     uint32_t q_vectors;                  // T * H * 8
     uint32_t B, T, H, freqs_rows, max_pages, num_pages, page_size;
     uint32_t kv_blocks;
+    uint32_t decode;  // T == B: try the one-token-per-request fast path first
     float eps, scale;
 };
 
@@ -87,51 +96,17 @@ __device__ __forceinline__ void store8(void* cache, int64_t elem, const float (&
     }
 }
 
-// One warp per token: RMSNorm of the latent part, RoPE of the rope part,
-// quantise, write the 576-wide cache row.
-// INPLACE: the latent row is not read from kv_in but from the cache slot
-// it is written back to (bf16, or E4M3 dequantised with the cache scale).
+// The row work of one warp once its slot is known: RMSNorm of the 512 latent
+// values (16 per lane), RoPE of the rope part (lanes 0..7, 4 adjacent pairs
+// each, freqs slice in fa/fb), quantisation and the store of the 576-wide
+// cache row at element offset `base`.  x0/x1/xr hold the input row (unused
+// when INPLACE: the row is read from its slot), g0/g1 this lane's gamma.
 template <bool FP8, bool INPLACE>
-__device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
-    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
-    const bool active = t < a.T;
-    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
-    if (INPLACE && active) {
-        g0 = ld_table(a.gamma + lane);
-        g1 = ld_table(a.gamma + 32 + lane);
-    } else if (active) {
-        const uint4* row = reinterpret_cast<const uint4*>(a.kv_in + (int64_t)t * a.kv_row_stride);
-        x0 = ld_stream(row + lane);
-        x1 = ld_stream(row + 32 + lane);
-        if (lane < 8) xr = ld_stream(row + 64 + lane);
-        g0 = ld_table(a.gamma + lane);
-        g1 = ld_table(a.gamma + 32 + lane);
-    }
-    if (!stage_tables(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
-        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
-        return;
-    }
-    if (!active) return;
-    const uint32_t b = find_request(s_off, a.B, t);
-    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-    if (pos >= a.freqs_rows) {
-        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
-        return;
-    }
-    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
-                                  a.s_token, a.layer_off, b, pos);
-    if (base < 0) {
-        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
-        return;
-    }
-    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
-    if (lane < 8) {
-        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
-        fa = ld_table(fr);
-        fb = ld_table(fr + 1);
-    }
-    // RMSNorm of the 512 latent values held 16 per lane.
+__device__ __forceinline__ void latent_row_compute(const MlaArgs& a, int64_t base, uint32_t lane,
+                                                   const uint4& x0, const uint4& x1,
+                                                   const uint4& xr, const uint4& g0,
+                                                   const uint4& g1, const float4& fa,
+                                                   const float4& fb) {
     float v0[8], v1[8], w0[8], w1[8], xv[8];
     if (INPLACE) {
         constexpr int64_t esz = FP8 ? 1 : 2;
@@ -170,6 +145,173 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         rope_pair(xv[6], xv[7], fb.z, fb.w, yr[6], yr[7]);
         store8<FP8>(a.cache, base + kNorm + lane * 8, yr, a.scale);
     }
+}
+
+// Input row (not INPLACE) and gamma slices of this lane.
+template <bool INPLACE>
+__device__ __forceinline__ void latent_row_loads(const MlaArgs& a, uint32_t t, uint32_t lane,
+                                                 uint4& x0, uint4& x1, uint4& xr, uint4& g0,
+                                                 uint4& g1) {
+    if (!INPLACE) {
+        const uint4* row = reinterpret_cast<const uint4*>(a.kv_in + (int64_t)t * a.kv_row_stride);
+        x0 = ld_stream(row + lane);
+        x1 = ld_stream(row + 32 + lane);
+        if (lane < 8) xr = ld_stream(row + 64 + lane);
+    }
+    g0 = ld_table(a.gamma + lane);
+    g1 = ld_table(a.gamma + 32 + lane);
+}
+
+// One warp per token: RMSNorm of the latent part, RoPE of the rope part,
+// quantise, write the 576-wide cache row.
+// INPLACE: the latent row is not read from kv_in but from the cache slot
+// it is written back to (bf16, or E4M3 dequantised with the cache scale).
+template <bool FP8, bool INPLACE>
+__device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, uint32_t* s_clen) {
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
+    const bool active = t < a.T;
+    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
+    if (active) latent_row_loads<INPLACE>(a, t, lane, x0, x1, xr, g0, g1);
+    if (!stage_tables(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    if (!active) return;
+    const uint32_t b = find_request(s_off, a.B, t);
+    const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+    if (pos >= a.freqs_rows) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
+        return;
+    }
+    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                                  a.s_token, a.layer_off, b, pos);
+    if (base < 0) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
+        return;
+    }
+    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+    if (lane < 8) {
+        const float4* fr = reinterpret_cast<const float4*>(a.freqs + pos * kRope) + lane * 2;
+        fa = ld_table(fr);
+        fb = ld_table(fr + 1);
+    }
+    latent_row_compute<FP8, INPLACE>(a, base, lane, x0, x1, xr, g0, g1, fa, fb);
+}
+
+// Whether input_row_offsets[i] == i for the entries this thread checks
+// (i = threadIdx.x, + blockDim.x, ... <= B); the loads are issued here and
+// the vote is taken later.
+__device__ __forceinline__ uint32_t identity_part(const uint32_t* __restrict__ offsets,
+                                                  uint32_t B) {
+    uint32_t ok = 1;
+    for (uint32_t i = threadIdx.x; i <= B; i += kThreads) ok &= __ldg(offsets + i) == i ? 1u : 0u;
+    return ok;
+}
+
+// Decode fast path of the latent CTAs (T == B).  Returns false, before
+// writing or flagging anything, when the offsets are not the identity; the
+// CTA then runs latent_rows.  Uniform across the CTA.
+template <bool FP8, bool INPLACE>
+__device__ __forceinline__ bool latent_rows_decode(const MlaArgs& a) {
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t t = blockIdx.x * kRowsPerKvBlock + warp;
+    const bool active = t < a.T;
+    const uint32_t ok = identity_part(a.offsets, a.B);
+    const uint32_t pos = active ? __ldg(a.cache_lengths + t) : 0u;
+    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
+    if (active) latent_row_loads<INPLACE>(a, t, lane, x0, x1, xr, g0, g1);
+    const bool pos_ok = pos < a.freqs_rows;
+    const uint32_t pidx = pos / a.page_size;
+    uint32_t page = KVW_PAGE_UNMAPPED;
+    float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
+    if (active && pos_ok) {
+        if (pidx < a.max_pages) page = __ldg(a.page_table + (uint64_t)t * a.max_pages + pidx);
+        if (lane < 8) {
+            const float4* fr =
+                reinterpret_cast<const float4*>(a.freqs + (uint64_t)pos * kRope) + lane * 2;
+            fa = ld_table(fr);
+            fb = ld_table(fr + 1);
+        }
+    }
+    if (!__syncthreads_and(ok)) return false;
+    if (!active) return true;
+    if (!pos_ok) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
+        return true;
+    }
+    if (page >= a.num_pages) {
+        if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
+        return true;
+    }
+    const int64_t base =
+        (int64_t)page * a.s_page + a.layer_off + (int64_t)(pos - pidx * a.page_size) * a.s_token;
+    latent_row_compute<FP8, INPLACE>(a, base, lane, x0, x1, xr, g0, g1, fa, fb);
+    return true;
+}
+
+// Rotation of one q_rope vector (8 columns, 4 adjacent pairs) and its store.
+template <bool QF8>
+__device__ __forceinline__ void q_vector_compute(const MlaArgs& a, uint32_t v, const uint4& x,
+                                                 const float4& fa, const float4& fb) {
+    float xv[8], y[8];
+    unpack8(x, xv);
+    rope_pair(xv[0], xv[1], fa.x, fa.y, y[0], y[1]);
+    rope_pair(xv[2], xv[3], fa.z, fa.w, y[2], y[3]);
+    rope_pair(xv[4], xv[5], fb.x, fb.y, y[4], y[5]);
+    rope_pair(xv[6], xv[7], fb.z, fb.w, y[6], y[7]);
+    if (QF8)
+        reinterpret_cast<uint2*>(a.q_out)[v] = pack8_e4m3(y);
+    else
+        st_stream(a.q_out + v, pack8_bf16(y));
+}
+
+// Decode fast path of the q CTAs (T == B), same contract as
+// latent_rows_decode.  Every token's first vector reports a bad position,
+// so the flag is raised once per token, as in q_rows.
+template <int VPT, bool QF8>
+__device__ __forceinline__ bool q_rows_decode(const MlaArgs& a) {
+    const uint32_t qb = blockIdx.x - a.kv_blocks;
+    const uint32_t vbase = qb * (kThreads * VPT);
+    const uint32_t vpt = a.H * 8u;  // vectors per token
+    const uint32_t ok = identity_part(a.offsets, a.B);
+    uint32_t pos[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const uint32_t v = vbase + threadIdx.x + i * kThreads;
+        pos[i] = v < a.q_vectors ? __ldg(a.cache_lengths + v / vpt) : 0xffffffffu;
+    }
+    uint4 x[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const uint32_t v = vbase + threadIdx.x + i * kThreads;
+        x[i] = v < a.q_vectors ? ld_stream(a.q_in + v) : make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t j = threadIdx.x & 7u;  // 8-column slice of the 64-wide head row
+    float4 fa[VPT], fb[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        fa[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        fb[i] = fa[i];
+        if (pos[i] < a.freqs_rows) {
+            const float4* fr =
+                reinterpret_cast<const float4*>(a.freqs + (uint64_t)pos[i] * kRope) + j * 2;
+            fa[i] = ld_table(fr);
+            fb[i] = ld_table(fr + 1);
+        }
+    }
+    if (!__syncthreads_and(ok)) return false;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const uint32_t v = vbase + threadIdx.x + i * kThreads;
+        if (v >= a.q_vectors) break;
+        if (pos[i] >= a.freqs_rows) {
+            if (v % vpt == 0u) flag(a.err_flags, KVW_ERR_POSITION);
+            continue;
+        }
+        q_vector_compute<QF8>(a, v, x[i], fa[i], fb[i]);
+    }
+    return true;
 }
 
 // q_rope streaming: VPT 16-byte vectors per thread.
@@ -225,16 +367,7 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
             }
         }
         if (p == 0xffffffffu) continue;
-        float xv[8], y[8];
-        unpack8(x[i], xv);
-        rope_pair(xv[0], xv[1], fa.x, fa.y, y[0], y[1]);
-        rope_pair(xv[2], xv[3], fa.z, fa.w, y[2], y[3]);
-        rope_pair(xv[4], xv[5], fb.x, fb.y, y[4], y[5]);
-        rope_pair(xv[6], xv[7], fb.z, fb.w, y[6], y[7]);
-        if (QF8)
-            reinterpret_cast<uint2*>(a.q_out)[v] = pack8_e4m3(y);
-        else
-            st_stream(a.q_out + v, pack8_bf16(y));
+        q_vector_compute<QF8>(a, v, x[i], fa, fb);
     }
 }
 
@@ -243,19 +376,24 @@ __global__ void __launch_bounds__(kThreads) mla_rope_rmsnorm_quant_kernel(const 
     extern __shared__ uint32_t s_dyn[];
     uint32_t* s_off = s_dyn;
     uint32_t* s_clen = s_dyn + a.B + 1;
-    if (blockIdx.x < a.kv_blocks)
+    // the fast path exists in the one-wave instances (VPT 1 and 2) a decode
+    // batch launches; the VPT 4 instances of long prefill launches keep their
+    // register count without it
+    constexpr bool kDecodePath = VPT <= 2;
+    if (blockIdx.x < a.kv_blocks) {
+        if (kDecodePath && a.decode && latent_rows_decode<FP8, INPLACE>(a)) return;
         latent_rows<FP8, INPLACE>(a, s_off, s_clen);
-    else
+    } else {
+        if (kDecodePath && a.decode && q_rows_decode<VPT, QF8>(a)) return;
         q_rows<VPT, QF8>(a, s_off, s_clen);
+    }
 }
 
 template <bool FP8, int VPT, bool QF8, bool INPLACE>
 cudaError_t launch(const MlaArgs& a, uint32_t blocks, size_t smem, cudaStream_t stream) {
-    auto k = mla_rope_rmsnorm_quant_kernel<FP8, VPT, QF8, INPLACE>;
-    if (smem > 32 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    constexpr auto k = mla_rope_rmsnorm_quant_kernel<FP8, VPT, QF8, INPLACE>;
+    const cudaError_t e = prepare_smem<k>(smem);
+    if (e != cudaSuccess) return e;
     k<<<blocks, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -263,14 +401,11 @@ cudaError_t launch(const MlaArgs& a, uint32_t blocks, size_t smem, cudaStream_t 
 // CTAs of this kernel that fit on the device at once (all SMs).
 template <bool FP8, int VPT, bool QF8, bool INPLACE>
 uint64_t resident_ctas(size_t smem) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, mla_rope_rmsnorm_quant_kernel<FP8, VPT, QF8, INPLACE>, kThreads, smem) !=
+    uint64_t n = 0;
+    if (wave_ctas<mla_rope_rmsnorm_quant_kernel<FP8, VPT, QF8, INPLACE>>(kThreads, smem, n) !=
         cudaSuccess)
         return 0;
-    return (uint64_t)sms * (uint64_t)per_sm;
+    return n;
 }
 
 // Grid sizing and launch of one instance.  Vectors per thread: the smallest
@@ -379,6 +514,7 @@ int mla_entry(void* q_rope_out, int32_t out_dtype, const void* q_rope,
     a.num_pages = cache->num_pages;
     a.page_size = cache->page_size;
     a.kv_blocks = (tot_seq_len + kRowsPerKvBlock - 1) / kRowsPerKvBlock;
+    a.decode = tot_seq_len == num_batches ? 1u : 0u;
     a.eps = epsilon;
     a.scale = cache->scale;
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);

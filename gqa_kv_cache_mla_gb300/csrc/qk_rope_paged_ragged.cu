@@ -71,6 +71,7 @@ struct GqaArgs {
     uint32_t stage_bytes, q_off, k_off, f_off, meta_off;  // stage layout
     uint32_t slices;            // head slices per (token, pair group)
     uint32_t items;             // (Hq + Hk) * S / 16 (register-staged kernel)
+    uint64_t wait_ns;           // limit of every mbarrier wait of the pipeline
 };
 
 __device__ __forceinline__ uint32_t section_of(const GqaArgs& a, uint32_t k) {
@@ -88,6 +89,10 @@ struct TokMeta {
     uint32_t pad;
 };
 
+// WITHHOLD (test builds only): the first group of every CTA is announced on
+// its stage barrier but none of its copies is issued, so the consumers' wait
+// for that stage runs into its limit.
+template <bool WITHHOLD>
 __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint64_t* empty,
                                          const uint32_t* s_off, const uint32_t* s_clen,
                                          unsigned char* stages) {
@@ -103,7 +108,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
         // them under the consumers' work.  With slot positions (one load) the
         // wait comes first: that order measured faster there.
         const bool early = a.mode != 0;
-        if (!early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+        if (!early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, a.wait_ns)) {
             if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
             break;
         }
@@ -128,7 +133,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
                 if (kbase >= 0) bytes += a.Hk * krow_bytes;
             }
         }
-        if (early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+        if (early && it >= (uint32_t)kStages && !mbar_wait(&empty[s], ph ^ 1u, a.wait_ns)) {
             if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
             break;
         }
@@ -145,6 +150,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
         __syncwarp();
         if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes + qbytes);
         __syncwarp();
+        if (WITHHOLD && it == 0) continue;
         if (lane == 0 && qbytes)
             bulk_load(st + a.q_off, a.q_in + (uint64_t)t0 * a.Hq * a.S, qbytes, &full[s]);
         // K rows: one copy per run of tokens whose rows are adjacent in the
@@ -192,7 +198,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
     // Do not leave the CTA with copies in flight: wait for the stages issued last.
     if (lane == 0) {
         for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0u; j < it; ++j)
-            if (!mbar_wait(&full[j % kStages], (j / kStages) & 1u, kWaitLimitNs))
+            if (!mbar_wait(&full[j % kStages], (j / kStages) & 1u, a.wait_ns))
                 flag(a.err_flags, KVW_ERR_TIMEOUT);
     }
 }
@@ -210,7 +216,7 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
     for (uint32_t g = blockIdx.x; g < a.groups; g += gridDim.x, ++it) {
         const uint32_t s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
-        if (!mbar_wait(&full[s], ph, kWaitLimitNs)) {
+        if (!mbar_wait(&full[s], ph, a.wait_ns)) {
             if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
             return;
         }
@@ -328,7 +334,7 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
     }
 }
 
-template <bool INTERLEAVED, bool FP8K>
+template <bool INTERLEAVED, bool FP8K, bool WITHHOLD>
 __global__ void __launch_bounds__(kThreads, 1) qk_rope_kernel(const GqaArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -349,23 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1) qk_rope_kernel(const GqaArgs a) {
         return;
     }
     if (threadIdx.x >= (unsigned)kConsumers)
-        producer(a, full, empty, s_off, s_clen, stages);
+        producer<WITHHOLD>(a, full, empty, s_off, s_clen, stages);
     else
         consumer<INTERLEAVED, FP8K>(a, full, empty, stages);
 }
 
-template <bool INTERLEAVED, bool FP8K>
+template <bool INTERLEAVED, bool FP8K, bool WITHHOLD = false>
 cudaError_t launch(const GqaArgs& a, size_t smem, cudaStream_t stream) {
-    auto k = qk_rope_kernel<INTERLEAVED, FP8K>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    constexpr auto k = qk_rope_kernel<INTERLEAVED, FP8K, WITHHOLD>;
+    uint64_t cap = 0;
+    const cudaError_t e = wave_ctas<k>(kThreads, smem, cap);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem)) != cudaSuccess)
-        return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    const uint64_t cap = (uint64_t)sms * per_sm;
+    if (cap == 0) return cudaErrorInvalidConfiguration;
     const uint32_t grid = (uint32_t)(a.groups < cap ? a.groups : cap);
     k<<<grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
@@ -567,20 +568,12 @@ __global__ void __launch_bounds__(1024) qk_rope_staged_kernel(const GqaArgs a) {
 
 template <bool INTERLEAVED, int TPB, bool FP8K>
 cudaError_t launch_staged(const GqaArgs& a, uint32_t threads, size_t smem, cudaStream_t stream) {
-    auto k = qk_rope_staged_kernel<INTERLEAVED, TPB, FP8K>;
-    cudaError_t e;
-    if (smem > 16 * 1024) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, smem)) != cudaSuccess)
-        return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    constexpr auto k = qk_rope_staged_kernel<INTERLEAVED, TPB, FP8K>;
+    uint64_t wave = 0;
+    const cudaError_t e = wave_ctas<k>((int)threads, smem, wave);
+    if (e != cudaSuccess) return e;
+    if (wave == 0) return cudaErrorInvalidConfiguration;
     const uint64_t groups = (a.T + TPB - 1) / TPB;
-    const uint64_t wave = (uint64_t)sms * per_sm;
     k<<<(uint32_t)(groups < wave ? groups : wave), threads, smem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -590,14 +583,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 }  // namespace kvw
 
-extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* input_row_offsets,
-                                        uint32_t num_batches, uint32_t tot_seq_len,
-                                        uint32_t num_q_heads, const kvw_paged_cache_t* cache,
-                                        const void* freqs_cis, uint32_t freqs_rows,
-                                        const uint32_t* position_ids, int interleaved,
-                                        const uint32_t* mrope_section, uint32_t layer_idx,
-                                        void* output, uint32_t* err_flags, cudaStream_t stream) {
-    using namespace kvw;
+namespace kvw {
+namespace {
+
+// Validation, sizing and launch.  `withhold` (test builds only) launches the
+// pipelined kernel with its first group's copies withheld; `wait_ns` bounds
+// every wait of the pipeline.
+int qk_entry(const void* q_proj, const uint32_t* input_row_offsets, uint32_t num_batches,
+             uint32_t tot_seq_len, uint32_t num_q_heads, const kvw_paged_cache_t* cache,
+             const void* freqs_cis, uint32_t freqs_rows, const uint32_t* position_ids,
+             int interleaved, const uint32_t* mrope_section, uint32_t layer_idx, void* output,
+             uint32_t* err_flags, cudaStream_t stream, bool withhold, uint64_t wait_ns) {
     if (!cache) return KVW_EINVAL;
     if (cache->dtype != KVW_DTYPE_BF16 && cache->dtype != KVW_DTYPE_FP8_E4M3)
         return KVW_EUNSUPPORTED;
@@ -663,14 +659,14 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     a.sec0 = sec0;
     a.sec01 = sec01;
     a.items = (uint32_t)items;
+    a.wait_ns = wait_ns;
+    if (withhold && a.mode == 2) return KVW_EUNSUPPORTED;  // the hook is in the pipeline only
     if (a.mode == 2) {
         const uint32_t threads = (uint32_t)((items + 31) / 32 * 32);
         const size_t smem_st = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
         // small batches: smaller groups, so that every SM gets a few of them
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return KVW_ECUDA;
+        int sms = 0;
+        if (sm_count(sms) != cudaSuccess) return KVW_ECUDA;
         int tpb = 4;
         while (tpb > 1 && (uint64_t)(tot_seq_len + tpb - 1) / tpb < (uint64_t)sms * 4) tpb >>= 1;
         cudaError_t es;
@@ -694,11 +690,8 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     const uint64_t per_tok = (uint64_t)num_q_heads * S * 2 + (uint64_t)a.Hk * S * esz +
                              (uint64_t)S * 4 +
                              sizeof(TokMeta);
-    int dev = 0, optin = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return KVW_ECUDA;
+    int optin = 0, sms = 0;
+    if (smem_optin(optin) != cudaSuccess || sm_count(sms) != cudaSuccess) return KVW_ECUDA;
     const uint64_t budget = (uint64_t)optin - 128 - tables - kStages * 1024;
     uint64_t tpb_max = budget / (kStages * per_tok);
     if (tpb_max > kMaxTPB) tpb_max = kMaxTPB;
@@ -749,9 +742,53 @@ extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* inpu
     if (a.slices > num_q_heads + a.Hk) a.slices = num_q_heads + a.Hk;
     const size_t smem = 128 + (size_t)tables + (size_t)kStages * a.stage_bytes;
     if (smem > (size_t)optin) return KVW_EUNSUPPORTED;
-    const cudaError_t e = interleaved ? (fp8 ? launch<true, true>(a, smem, stream)
-                                             : launch<true, false>(a, smem, stream))
-                                      : (fp8 ? launch<false, true>(a, smem, stream)
-                                             : launch<false, false>(a, smem, stream));
+    cudaError_t e;
+#ifdef KVW_TEST_HOOKS
+    if (withhold)
+        e = interleaved ? (fp8 ? launch<true, true, true>(a, smem, stream)
+                               : launch<true, false, true>(a, smem, stream))
+                        : (fp8 ? launch<false, true, true>(a, smem, stream)
+                               : launch<false, false, true>(a, smem, stream));
+    else
+#else
+    if (withhold) return KVW_EUNSUPPORTED;
+#endif
+        e = interleaved ? (fp8 ? launch<true, true>(a, smem, stream)
+                               : launch<true, false>(a, smem, stream))
+                        : (fp8 ? launch<false, true>(a, smem, stream)
+                               : launch<false, false>(a, smem, stream));
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }
+
+}  // namespace
+}  // namespace kvw
+
+extern "C" int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* input_row_offsets,
+                                        uint32_t num_batches, uint32_t tot_seq_len,
+                                        uint32_t num_q_heads, const kvw_paged_cache_t* cache,
+                                        const void* freqs_cis, uint32_t freqs_rows,
+                                        const uint32_t* position_ids, int interleaved,
+                                        const uint32_t* mrope_section, uint32_t layer_idx,
+                                        void* output, uint32_t* err_flags, cudaStream_t stream) {
+    return kvw::qk_entry(q_proj, input_row_offsets, num_batches, tot_seq_len, num_q_heads, cache,
+                         freqs_cis, freqs_rows, position_ids, interleaved, mrope_section,
+                         layer_idx, output, err_flags, stream, false, kvw::kWaitLimitNs);
+}
+
+#ifdef KVW_TEST_HOOKS
+// Test builds only (compiled with -DKVW_TEST_HOOKS into a separate library;
+// the product library has no such symbol): the pipelined GQA kernel with the
+// first group of every CTA announced on its stage barrier but never copied,
+// and every wait bounded by `wait_ns`, so the consumers' wait for that stage
+// runs out, KVW_ERR_TIMEOUT is set and the kernel returns.
+extern "C" int kvw_test_qk_rope_withheld_stage(
+    const void* q_proj, const uint32_t* input_row_offsets, uint32_t num_batches,
+    uint32_t tot_seq_len, uint32_t num_q_heads, const kvw_paged_cache_t* cache,
+    const void* freqs_cis, uint32_t freqs_rows, const uint32_t* position_ids, int interleaved,
+    uint32_t layer_idx, void* output, uint32_t* err_flags, cudaStream_t stream,
+    uint64_t wait_ns) {
+    return kvw::qk_entry(q_proj, input_row_offsets, num_batches, tot_seq_len, num_q_heads, cache,
+                         freqs_cis, freqs_rows, position_ids, interleaved, nullptr, layer_idx,
+                         output, err_flags, stream, true, wait_ns);
+}
+#endif

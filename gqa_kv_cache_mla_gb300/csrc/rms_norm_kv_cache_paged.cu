@@ -191,21 +191,15 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
 
 template <int VPL, int RPT, bool MBC, bool FULL>
 cudaError_t launch_one(const KnArgs& a, size_t smem, cudaStream_t stream) {
-    auto k = rms_norm_kv_kernel<VPL, RPT, MBC, FULL>;
-    if (smem > 32 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    constexpr auto k = rms_norm_kv_kernel<VPL, RPT, MBC, FULL>;
     const uint32_t rows_wt = (32u >> a.tl_log2) * RPT;
     const uint32_t wtiles = (a.rows + rows_wt - 1) / rows_wt;
     const uint32_t tiles = (wtiles + kThreads / 32 - 1) / (kThreads / 32);  // CTAs with work
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    uint64_t wave = 0;
+    const cudaError_t e = wave_ctas<k>(kThreads, smem, wave);
     if (e != cudaSuccess) return e;
-    const uint32_t wave = (uint32_t)sms * (uint32_t)(per_sm > 0 ? per_sm : 1);
-    k<<<tiles < wave ? tiles : wave, kThreads, smem, stream>>>(a);
+    if (wave == 0) return cudaErrorInvalidConfiguration;
+    k<<<tiles < wave ? tiles : (uint32_t)wave, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -39,9 +39,15 @@
  *     KVW_ERR_OFFSETS  input_row_offsets does not start at 0, does not end
  *                      at the token count, or decreases: nothing is written.
  *     KVW_ERR_TIMEOUT  an internal pipeline wait (between the copy engine
- *                      and the compute warps of one CTA) gave up after about
- *                      one second; the output is incomplete.  Never expected;
- *                      reported instead of hanging the GPU.
+ *                      and the compute warps of one CTA of the GQA kernel)
+ *                      gave up after about one second of GPU time; the
+ *                      output is incomplete.  Reported instead of hanging
+ *                      the GPU.  It is not expected on a healthy device, but
+ *                      a CTA that the GPU pre-empts for longer than the
+ *                      limit (time slicing with other processes on a shared
+ *                      GPU) can report it spuriously.  With err_flags NULL
+ *                      a timeout goes unnoticed: pass a flag word wherever
+ *                      incomplete output must be detected.
  *   With zero tokens nothing is launched and nothing is checked.
  * - Ragged batches: input_row_offsets (device, uint32 [num_batches + 1])
  *   marks request boundaries in the flattened token dimension; request b

@@ -166,6 +166,76 @@ def test_mla_empty_and_repeat(orc, dev):
     assert np.array_equal(a[0], d.q_out.host()) and np.array_equal(a[1], d.cache.host())
 
 
+# ------------------------------------------------- MLA decode batches (T == B)
+# With as many tokens as requests the kernel first assumes the offsets are
+# the identity (one token per request) and verifies that over the whole
+# table; any other table takes the general path.  Both must give the
+# oracle's results and flags.
+
+@pytest.mark.parametrize("B,H", [(1, 128), (5, 3), (13, 1), (700, 2), (300, 0)])
+@pytest.mark.parametrize("dtype", [W.DTYPE_FP8_E4M3, W.DTYPE_BF16])
+def test_mla_decode_identity_shapes(orc, dev, B, H, dtype):
+    rng = np.random.default_rng(1000 + B + H)
+    prior = rng.integers(0, 900, B)
+    w = W.mla_workload("dec", 1001 + B, np.ones(B, np.int64), prior, num_heads=H,
+                       page_size=16, max_seq_len=1024, cache_dtype=dtype, num_layers=2,
+                       layer_idx=1)
+    run_mla(orc, dev, w)
+
+
+@pytest.mark.parametrize("variant", ["inplace", "fp8q"])
+def test_mla_decode_identity_variants(orc, dev, variant):
+    rng = np.random.default_rng(1010)
+    B = 37
+    w = W.mla_workload("decv", 1011, np.ones(B, np.int64), rng.integers(0, 500, B),
+                       num_heads=5, page_size=32, max_seq_len=512,
+                       cache_dtype=W.DTYPE_FP8_E4M3)
+    if variant == "inplace":
+        w = W.mla_inplace(w)
+    else:
+        w.q_out_dtype = W.DTYPE_FP8_E4M3
+    run_mla(orc, dev, w)
+
+
+def test_mla_decode_count_but_not_identity(orc, dev):
+    # T == B, valid offsets, but requests with 0 and 2+ new tokens
+    new = np.array([2, 0, 1, 1, 3, 0, 0, 1])
+    w = W.mla_workload("dni", 1021, new, [5, 0, 17, 3, 40, 9, 0, 2], num_heads=3,
+                       page_size=16, max_seq_len=128, cache_dtype=W.DTYPE_FP8_E4M3)
+    assert w.T == w.B
+    run_mla(orc, dev, w)
+
+
+def test_mla_decode_identity_flags(orc, dev):
+    import torch
+
+    B = 40
+    prior = np.arange(B) * 3
+    # positions past the table for the last requests
+    w = W.mla_workload("dfp", 1031, np.ones(B, np.int64), prior, num_heads=4, page_size=16,
+                       max_seq_len=128, cache_dtype=W.DTYPE_BF16)
+    w.freqs = w.freqs[:100].copy()
+    d, _, _ = run_mla(orc, dev, w)
+    assert d.flags() == 2
+    # an unmapped page
+    w = W.mla_workload("dfg", 1032, np.ones(B, np.int64), prior, num_heads=4, page_size=16,
+                       max_seq_len=128, cache_dtype=W.DTYPE_FP8_E4M3)
+    w.cache.page_table[7, prior[7] // 16] = W.PAGE_UNMAPPED  # the page of request 7's token
+    d, _, _ = run_mla(orc, dev, w)
+    assert d.flags() == 1
+    # T == B but the offsets are not a valid table: nothing is written
+    for bad in ([0, 1, 1, 0, 4], [0, 1, 2, 3, 5], [1, 1, 2, 3, 4]):
+        w = W.mla_workload("dbo", 1033, np.ones(4, np.int64), [3, 1, 4, 1], num_heads=2,
+                           page_size=16, max_seq_len=64, cache_dtype=W.DTYPE_FP8_E4M3)
+        w.offsets = np.array(bad, np.uint32)
+        d = dev.DeviceMLA(w)
+        d.run(tot_seq_len=4)
+        torch.cuda.synchronize()
+        assert d.flags() == 4
+        assert np.array_equal(d.cache.host(), w.cache.data)
+        assert np.array_equal(d.q_out.host(), d.q_out_init)
+
+
 # ------------------------------------------------------------------ GQA
 
 def run_gqa(orc, dev, w, alias=False):
