@@ -347,7 +347,8 @@ class Flusher:
         self.fr.sum()
 
 
-def measure(name, steps, warmup, dev, rank, world, flusher, e2e=True, cpu_s=None):
+def measure(name, steps, warmup, dev, rank, world, flusher, e2e=True, cpu_s=None,
+            host_timing=True):
     """Device-timed throughput of one workload (and optionally its end-to-end
     figure and the oracle beside it).  Returns the fields of a bench line."""
     import torch
@@ -426,7 +427,8 @@ def measure(name, steps, warmup, dev, rank, world, flusher, e2e=True, cpu_s=None
             "frac": achieved / peak, "traffic": ncu_traffic(name, kfile),
             "algorithmic_bytes": abytes, "peak_source": peak_src,
             "kernel": kfile.replace(".cu", "")}
-    host_us = host_call_us(run, stream) if name in ("mla_decode",) else None
+    host_us = (host_call_us(run, stream) if name in ("mla_decode",) and host_timing
+               else None)
     if k == "mla" and w.inplace:
         d.cache.reset(w.cache.data)
     cpu = None
@@ -457,14 +459,16 @@ def run_ours(args):
 
     flusher = Flusher(dev)
     main_r = measure(args.workload, args.steps, args.warmup, dev, rank, world, flusher,
-                     e2e=not args.no_e2e, cpu_s=None if args.no_cpu_baseline else args.cpu_s)
+                     e2e=not args.no_e2e, cpu_s=None if args.no_cpu_baseline else args.cpu_s,
+                     host_timing=not args.no_host_timing)
     also = []
     for name in args.also:
         if name == args.workload:
             continue
         steps = args.also_steps or default_steps(name)
         r = measure(name, steps, args.warmup, dev, rank, world, flusher,
-                    e2e=not args.no_e2e and name in ("mla_decode",), cpu_s=None)
+                    e2e=not args.no_e2e and name in ("mla_decode",), cpu_s=None,
+                    host_timing=not args.no_host_timing)
         also.append({"workload": r["config"]["workload"], "value": r["value"],
                      "unit": r["unit"], "ms_per_step": r["ms_per_step"], "steps": steps,
                      "roofline": {x: r["roofline"][x] for x in
@@ -761,6 +765,8 @@ def main():
                     help="timed steps of each 'also' workload (default: its own count)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-host-timing", action="store_true",
+                    help="skip the host-time-per-call measurement of the decode call")
     ap.add_argument("--cpu-s", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--ref-step-s", type=float, default=2.0,

@@ -192,8 +192,19 @@ __device__ __forceinline__ uint2 quantize_piece(const uint4& raw, float cache_sc
     float v[8];
     to_f32<CF8>(raw, cache_scale, v);
     if (fast) {
+        // div_refined on fp32 pairs: the packed multiply and fused
+        // multiply-add round each component exactly as the scalar ones, and
+        // x - q0 s is formed as fma(q0, -s, x)
+        const float2 ns2 = make_float2(-sc, -sc), y2 = make_float2(y, y);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = div_refined(v[e], sc, y);
+        for (int e = 0; e < 8; e += 2) {
+            const float2 x2 = make_float2(v[e], v[e + 1]);
+            const float2 q0 = __fmul2_rn(x2, y2);
+            const float2 r = __ffma2_rn(q0, ns2, x2);
+            const float2 q = __ffma2_rn(r, y2, q0);
+            v[e] = copysignf(q.x, x2.x);
+            v[e + 1] = copysignf(q.y, x2.y);
+        }
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(v[e], sc);

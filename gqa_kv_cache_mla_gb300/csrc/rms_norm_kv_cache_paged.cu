@@ -31,6 +31,7 @@ constexpr uint32_t kThreads = 256;
 constexpr uint32_t kMaxCols = 2048;
 constexpr uint32_t kMaxWarpTileTokens = 66;  // tokens of a warp tile: up to 64 rows + 2
 
+
 struct KnArgs {
     uint16_t* cache;
     const uint32_t* offsets;
@@ -46,6 +47,7 @@ struct KnArgs {
     uint32_t nv;              // 16-byte vectors per row = ceil(G / 8)
     uint32_t rows;            // T * rows_per_token
     float eps, wo;
+    float inv_g;              // 1 / gamma_len (rounded)
     int mbc;
 };
 
@@ -189,6 +191,192 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
     }
 }
 
+// Fast path for contiguous rows: the normalised columns of a row are adjacent
+// in memory (per-head norm, or the whole K row of a token whose heads are
+// adjacent) and gamma_len is a multiple of 8.  The team geometry (TL lanes,
+// VPL 16-byte vectors per lane, RPT rows per team) is compile-time, so lane
+// tl of a team owns columns 8 (tl + v TL) .. + 7 of every row of the launch:
+// a row is one base pointer plus constant offsets and the team reduction
+// unrolls.  The sum of squares runs as VPL independent fused multiply-add
+// chains; team lane q computes the 1/rms of row q of its team (rsqrt refined
+// by one Newton-Raphson step, r' = r (3 - m r^2) / 2, within two fp32 ulp of
+// the correctly rounded value, so a bf16 result differs from a correctly
+// rounded reference by at most one ulp, on a few elements in 10^5) and the
+// team reads the values back with shuffles.  Slot resolution, tiling and the
+// per-warp walk are those of rms_norm_kv_kernel.
+// Exact bf16 widening by byte permutes: the same values as unpack8, from a
+// different instruction sequence.  The sum-of-squares pass uses this one and
+// the output pass unpack8, so the compiler re-widens the packed rows for the
+// output pass instead of keeping every widened value of the tile live across
+// the team reduction.
+__device__ __forceinline__ void unpack8_perm(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(__byte_perm(w[i], 0u, 0x1044u));
+        f[2 * i + 1] = __uint_as_float(__byte_perm(w[i], 0u, 0x3244u));
+    }
+}
+
+template <int TL, int VPL, int RPT, bool MBC>
+__global__ void __launch_bounds__(kThreads, 3) rms_norm_rows_kernel(const KnArgs a) {
+    static_assert(RPT <= TL, "a team lane computes the 1/rms of one row of its team");
+    constexpr uint32_t kTeams = 32u / TL;
+    constexpr uint32_t kRowsWt = kTeams * RPT;  // rows of a warp tile
+    constexpr uint32_t kCols = TL * VPL * 8;     // columns a team covers
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t* s_off = s_dyn;
+    uint32_t* s_clen = s_dyn + a.B + 1;
+    __shared__ int64_t s_wbase[kThreads / 32][kRowsWt + 2];
+    __shared__ __align__(16) float s_w[kCols];
+
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t team = lane / TL, tl = lane % TL;
+    // weights gamma + weight_offset of the normalised columns (zero past
+    // gamma_len, whose vectors are never loaded, normalised or stored)
+    for (uint32_t c = threadIdx.x; c < kCols; c += kThreads)
+        s_w[c] = c < a.G ? __fadd_rn(bf16_lo(__ldg(a.gamma + c)), a.wo) : 0.0f;
+    if (!stage_ragged(a.offsets, a.cache_lengths, a.B, a.T, s_off, s_clen)) {
+        if (threadIdx.x == 0) flag(a.err_flags, KVW_ERR_OFFSETS);
+        return;
+    }
+    const uint32_t wtiles = (a.rows + kRowsWt - 1) / kRowsWt;
+    const uint32_t nwarps = gridDim.x * (kThreads / 32);
+    int64_t* wbase = s_wbase[warp];
+    auto resolve = [&](uint32_t wt) {
+        const uint32_t r0 = wt * kRowsWt;
+        const uint32_t t_lo = r0 / a.rows_per_token;
+        const uint32_t t_hi = (min(r0 + kRowsWt, a.rows) - 1) / a.rows_per_token;
+        for (uint32_t k = lane; k <= t_hi - t_lo; k += 32) {
+            const uint32_t t = t_lo + k;
+            const uint32_t b = find_request(s_off, a.B, t);
+            const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
+            const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size,
+                                          a.s_page, a.s_token, a.layer_off, b, pos);
+            wbase[k] = base;
+            if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
+        }
+    };
+    uint32_t wt = blockIdx.x * (kThreads / 32) + warp;
+    if (wt < wtiles) resolve(wt);
+    __syncwarp();
+
+    const uint32_t nvec = a.nv;
+    for (; wt < wtiles; wt += nwarps) {
+        const uint32_t r0 = wt * kRowsWt;
+        const uint32_t t_lo = r0 / a.rows_per_token;
+        const uint32_t r_end = min(r0 + kRowsWt, a.rows);
+        // row r = r0 + team + q * kTeams, walked as (token, head) without dividing
+        uint16_t* ptr[RPT];
+        uint4 x[RPT][VPL];
+        uint32_t t = (r0 + team) / a.rows_per_token;
+        uint32_t g = (r0 + team) - t * a.rows_per_token;
+        const uint32_t dt = kTeams / a.rows_per_token, dg = kTeams - dt * a.rows_per_token;
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const uint32_t r = r0 + team + q * kTeams;
+            ptr[q] = nullptr;
+            if (r < r_end) {
+                const int64_t base = wbase[t - t_lo];
+                if (base >= 0) ptr[q] = a.cache + base + (int64_t)g * a.s_head + tl * 8u;
+            }
+            t += dt;
+            g += dg;
+            if (g >= a.rows_per_token) {
+                g -= a.rows_per_token;
+                ++t;
+            }
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                x[q][v] = make_uint4(0, 0, 0, 0);
+                if (ptr[q] && tl + v * TL < nvec)
+                    x[q][v] = *reinterpret_cast<const uint4*>(ptr[q] + v * TL * 8);
+            }
+        }
+        __syncwarp();  // every lane has read this tile's slots
+        if (wt + nwarps < wtiles) resolve(wt + nwarps);
+        __syncwarp();  // the next tile's slots are visible to the whole warp
+
+        // sums of squares of the RPT rows, completed across the team
+        float ss[RPT];
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            float part[VPL];
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                float xs[8];
+                unpack8_perm(x[q][v], xs);
+                part[v] = __fmul_rn(xs[0], xs[0]);
+#pragma unroll
+                for (int e = 1; e < 8; ++e) part[v] = __fmaf_rn(xs[e], xs[e], part[v]);
+            }
+#pragma unroll
+            for (int v = 1; v < VPL; ++v) part[0] = __fadd_rn(part[0], part[v]);
+            ss[q] = part[0];
+#pragma unroll
+            for (int o = TL / 2; o > 0; o >>= 1)
+                ss[q] = __fadd_rn(ss[q], __shfl_xor_sync(0xffffffffu, ss[q], o));
+        }
+        // one correctly rounded 1/rms per row: team lane q computes row q's
+        // and the team reads them back, instead of every lane computing all
+        float mine = ss[0];
+#pragma unroll
+        for (int q = 1; q < RPT; ++q)
+            if (tl == (uint32_t)q) mine = ss[q];
+        const float m = __fadd_rn(__fmul_rn(mine, a.inv_g), a.eps);
+        const float est = rsqrtf(m);
+        const float rinv_mine = __fmul_rn(est, __fmaf_rn(__fmul_rn(-0.5f, m) * est, est, 1.5f));
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const float rinv = __shfl_sync(0xffffffffu, rinv_mine, (lane & ~(TL - 1u)) | q);
+            if (!ptr[q]) continue;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                if (tl + v * TL >= nvec) continue;
+                const float4 w0 = *reinterpret_cast<const float4*>(s_w + (tl + v * TL) * 8u);
+                const float4 w1 = *reinterpret_cast<const float4*>(s_w + (tl + v * TL) * 8u + 4);
+                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                float xs[8], y[8];
+                unpack8(x[q][v], xs);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float xr = __fmul_rn(xs[e], rinv);
+                    y[e] = MBC ? __fmul_rn(xr, wv[e])
+                               : __fmul_rn(__bfloat162float(__float2bfloat16_rn(xr)), wv[e]);
+                }
+                *reinterpret_cast<uint4*>(ptr[q] + v * TL * 8) = pack8_bf16(y);
+            }
+        }
+    }
+}
+
+template <int TL, int VPL, int RPT, bool MBC>
+cudaError_t launch_rows(const KnArgs& a, size_t smem, cudaStream_t stream) {
+    constexpr auto k = rms_norm_rows_kernel<TL, VPL, RPT, MBC>;
+    constexpr uint32_t rows_wt = (32u / TL) * RPT;
+    const uint32_t wtiles = (a.rows + rows_wt - 1) / rows_wt;
+    const uint32_t tiles = (wtiles + kThreads / 32 - 1) / (kThreads / 32);  // CTAs with work
+    uint64_t wave = 0;
+    const cudaError_t e = wave_ctas<k>(kThreads, smem, wave);
+    if (e != cudaSuccess) return e;
+    if (wave == 0) return cudaErrorInvalidConfiguration;
+    k<<<tiles < wave ? tiles : (uint32_t)wave, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// Team geometry of the contiguous-row path from the 16-byte vectors per row
+// (nv <= 128): narrow teams for short rows, so that one instruction stream
+// serves several rows and every lane keeps a few vectors in flight.
+template <bool MBC>
+cudaError_t launch_rows_for(const KnArgs& a, size_t smem, cudaStream_t stream) {
+    if (a.nv <= 4) return launch_rows<4, 1, 4, MBC>(a, smem, stream);
+    if (a.nv <= 8) return launch_rows<4, 2, 4, MBC>(a, smem, stream);
+    if (a.nv <= 16) return launch_rows<4, 4, 2, MBC>(a, smem, stream);
+    if (a.nv <= 32) return launch_rows<8, 4, 2, MBC>(a, smem, stream);
+    if (a.nv <= 64) return launch_rows<16, 4, 2, MBC>(a, smem, stream);
+    return launch_rows<32, 4, 1, MBC>(a, smem, stream);
+}
+
 template <int VPL, int RPT, bool MBC, bool FULL>
 cudaError_t launch_one(const KnArgs& a, size_t smem, cudaStream_t stream) {
     constexpr auto k = rms_norm_kv_kernel<VPL, RPT, MBC, FULL>;
@@ -281,10 +469,17 @@ extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const
     a.rows = (uint32_t)rows;
     a.eps = epsilon;
     a.wo = weight_offset;
+    a.inv_g = 1.0f / (float)gamma_len;
     a.mbc = multiply_before_cast ? 1 : 0;
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);
     cudaError_t e;
-    if (vpl <= 1)
+    // contiguous rows of whole vectors take the fast path; gamma lengths that
+    // are not a multiple of 8 and whole K rows of padded heads the general one
+    const bool contiguous = per_head_norm || cache->num_heads == 1 ||
+                            cache->stride_head == (int64_t)S;
+    if (contiguous && gamma_len % 8 == 0 && a.nv <= 128)
+        e = a.mbc ? launch_rows_for<true>(a, smem, stream) : launch_rows_for<false>(a, smem, stream);
+    else if (vpl <= 1)
         e = launch<1, 8>(a, smem, stream);
     else if (vpl <= 2)
         e = launch<2, 4>(a, smem, stream);

@@ -338,8 +338,8 @@ def run_knorm(orc, dev, w, per_head_norm=True):
 def knorm_cast_first_ulp(w):
     """Tolerance of multiply_before_cast=false, which rounds twice: y1 = bf16(x*r),
     then bf16(y1*wt) with wt = gamma + weight_offset.  The kernel sums the
-    squares in another order, so r can differ in its last fp32 bits and y1 by
-    one bf16 ulp u1; the products then differ by |wt|*u1.  For |wt| >= 1 the
+    squares in another order and refines an rsqrt estimate of 1/rms, so r can
+    differ in its last fp32 bits and y1 by one bf16 ulp u1; the products then differ by |wt|*u1.  For |wt| >= 1 the
     result's ulp is at least u1 (and at least |wt|*u1/2), so the exact products
     differ by less than 2 result ulps and the rounded ones by at most 2; for
     |wt| < 1 the result's ulp can be as small as |wt|*u1/2, giving at most 3."""
