@@ -11,7 +11,8 @@
 // register-staged kernel further down): a persistent, warp-specialised TMA
 // pipeline.
 //   * The tokens are cut into groups of TPB consecutive tokens; each CTA (one
-//     per SM, sized by shared memory) walks groups blockIdx.x, + gridDim.x, ...
+//     per SM for a bf16 K cache, two for an E4M3 one, sized by shared memory)
+//     walks groups blockIdx.x, + gridDim.x, ...
 //   * A producer warp resolves each group's tokens (request by binary search
 //     in the staged offsets, slot position, RoPE positions, page id) and
 //     issues bulk (TMA) copies into a 2-stage shared-memory ring: the group's
@@ -334,8 +335,14 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
     }
 }
 
+// CTAs per SM: one for a bf16 K cache; two for an E4M3 K cache, whose
+// consumers spend more instructions per byte (decode, re-encode) and keep up
+// better with two CTAs' warps interleaved (stages sized for two CTAs).
+template <bool FP8K>
+constexpr int kCtasPerSm = FP8K ? 2 : 1;
+
 template <bool INTERLEAVED, bool FP8K, bool WITHHOLD>
-__global__ void __launch_bounds__(kThreads, 1) qk_rope_kernel(const GqaArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8K>) qk_rope_kernel(const GqaArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kStages;
@@ -692,7 +699,10 @@ int qk_entry(const void* q_proj, const uint32_t* input_row_offsets, uint32_t num
                              sizeof(TokMeta);
     int optin = 0, sms = 0;
     if (smem_optin(optin) != cudaSuccess || sm_count(sms) != cudaSuccess) return KVW_ECUDA;
-    const uint64_t budget = (uint64_t)optin - 128 - tables - kStages * 1024;
+    // shared memory of one CTA: an SM holds 1 (bf16 K) or 2 (E4M3 K) CTAs, each
+    // with 1 KiB reserved by the runtime
+    const uint64_t ctas = fp8 ? 2 : 1;
+    const uint64_t budget = ((uint64_t)optin + 1024) / ctas - 1024 - 128 - tables - kStages * 1024;
     uint64_t tpb_max = budget / (kStages * per_tok);
     if (tpb_max > kMaxTPB) tpb_max = kMaxTPB;
     // small batches: spread the groups over all SMs

@@ -389,6 +389,23 @@ def test_knorm_error_flags(orc, dev):
     assert d.flags() == 1
 
 
+@pytest.mark.parametrize("G", [128, 64])
+def test_knorm_full_with_bad_pages(orc, dev, G):
+    """The benchmark batch with an unmapped page and a page id past the cache.
+    With G = 128 the warps walk more than two tiles each, so the kernel reads
+    the page table from its shared-memory copy; with G = 64 from global."""
+    w = W.knorm_paged(gamma_len=G)
+    c = w.cache
+    lens = np.diff(w.offsets.astype(np.int64))
+    b1, b2 = [int(b) for b in np.flatnonzero(lens > 200)[:2]]
+    p1 = int(c.cache_lengths[b1]) // c.page_size + 1
+    p2 = int(c.cache_lengths[b2]) // c.page_size + 2
+    c.page_table[b1, p1] = W.PAGE_UNMAPPED
+    c.page_table[b2, p2] = c.num_pages + 5
+    d = run_knorm(orc, dev, w)
+    assert d.flags() == 1
+
+
 # ------------------------------------------------------------ padded layouts, small batches
 
 @pytest.mark.parametrize("kind", ["mla", "gqa", "gqa_mrope", "knorm"])
