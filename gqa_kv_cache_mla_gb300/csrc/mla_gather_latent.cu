@@ -185,12 +185,37 @@ __device__ __forceinline__ uint32_t piece_max_bits(const uint4& raw, float cache
     return __float_as_uint(f);
 }
 
+// Per-halfword maxima of the sign-cleared bf16 patterns of a piece, merged
+// into acc (bf16 magnitudes order like their patterns).
+__device__ __forceinline__ uint32_t halves_max(uint32_t acc, const uint4& raw) {
+    return __vmaxu2(acc, __vmaxu2(__vmaxu2(raw.x & 0x7fff7fffu, raw.y & 0x7fff7fffu),
+                                  __vmaxu2(raw.z & 0x7fff7fffu, raw.w & 0x7fff7fffu)));
+}
+
 // 8 cache values -> 8 E4M3 codes of value / sc (y = RN(1/sc); see div_refined).
 template <bool CF8>
 __device__ __forceinline__ uint2 quantize_piece(const uint4& raw, float cache_scale, float sc,
                                                 float y, bool fast) {
     float v[8];
     to_f32<CF8>(raw, cache_scale, v);
+    if (!CF8 && fast) {
+        // magnitudes divided on fp32 pairs, codes of the magnitudes, then the
+        // bf16 sign bits (byte 1 and 3 of each word) or-ed into the code bytes
+        const float2 ns2 = make_float2(-sc, -sc), y2 = make_float2(y, y);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const float2 x2 = make_float2(fabsf(v[e]), fabsf(v[e + 1]));
+            const float2 q0 = __fmul2_rn(x2, y2);
+            const float2 r = __ffma2_rn(q0, ns2, x2);
+            const float2 q = __ffma2_rn(r, y2, q0);
+            v[e] = q.x;
+            v[e + 1] = q.y;
+        }
+        uint2 c = pack8_e4m3(v);
+        c.x |= __byte_perm(raw.x, raw.y, 0x7531u) & 0x80808080u;
+        c.y |= __byte_perm(raw.z, raw.w, 0x7531u) & 0x80808080u;
+        return c;
+    }
     if (fast) {
         // div_refined on fp32 pairs: the packed multiply and fused
         // multiply-add round each component exactly as the scalar ones, and
@@ -255,16 +280,37 @@ __global__ void __launch_bounds__(kThreads, 3) gather_dynamic_kernel(const Gathe
                                                       : -1;
         // row maxima as bit patterns of non-negative floats (which order like
         // the values): per lane, then one redux over the warp per row
-        uint32_t mtail = btail >= 0 ? piece_max_bits<CF8>(rtail, a.cache_scale) : 0u;
         uint32_t mbits[kDynRows];
+        if constexpr (!CF8) {
+            const uint32_t atail = btail >= 0 ? halves_max(0u, rtail) : 0u;
 #pragma unroll
-        for (uint32_t q = 0; q < kDynRows; ++q) {
-            uint32_t mq = tq == q ? mtail : 0u;
-            if (base[q] >= 0) {
-                mq = max(mq, piece_max_bits<CF8>(raw[q][0], a.cache_scale));
-                mq = max(mq, piece_max_bits<CF8>(raw[q][1], a.cache_scale));
+            for (uint32_t q = 0; q < kDynRows; ++q) {
+                uint32_t acc = tq == q ? atail : 0u;
+                if (base[q] >= 0) acc = halves_max(halves_max(acc, raw[q][0]), raw[q][1]);
+                uint32_t mq = max(acc & 0xffffu, acc >> 16);
+                if (mq > 0x7f80u) {  // a NaN among this lane's values of row q: float maximum
+                    float f = 0.0f;
+                    if (base[q] >= 0) f = fmaxf(__uint_as_float(piece_max_bits<CF8>(raw[q][0], 1.0f)),
+                                                __uint_as_float(piece_max_bits<CF8>(raw[q][1], 1.0f)));
+                    if (tq == q && btail >= 0)
+                        f = fmaxf(f, __uint_as_float(piece_max_bits<CF8>(rtail, 1.0f)));
+                    mq = __float_as_uint(f);
+                } else {
+                    mq <<= 16;
+                }
+                mbits[q] = __reduce_max_sync(0xffffffffu, mq);
             }
-            mbits[q] = __reduce_max_sync(0xffffffffu, mq);
+        } else {
+            uint32_t mtail = btail >= 0 ? piece_max_bits<CF8>(rtail, a.cache_scale) : 0u;
+#pragma unroll
+            for (uint32_t q = 0; q < kDynRows; ++q) {
+                uint32_t mq = tq == q ? mtail : 0u;
+                if (base[q] >= 0) {
+                    mq = max(mq, piece_max_bits<CF8>(raw[q][0], a.cache_scale));
+                    mq = max(mq, piece_max_bits<CF8>(raw[q][1], a.cache_scale));
+                }
+                mbits[q] = __reduce_max_sync(0xffffffffu, mq);
+            }
         }
         // lane q turns row q's maximum into its scale and reciprocal
         uint32_t mine = mbits[0];

@@ -633,6 +633,50 @@ def test_gather_dynamic_outliers_and_zero_rows(orc, dev):
     run_gather(orc, dev, g)
 
 
+@pytest.mark.parametrize("cache_dtype", [W.DTYPE_BF16, W.DTYPE_FP8_E4M3])
+def test_gather_dynamic_nan_values(orc, dev, cache_dtype):
+    """NaN values in cached rows: the row maximum ignores them (as the
+    reference maximum does), so the scales and every code of a non-NaN value
+    match the reference bit for bit; a NaN value gives a NaN code (E4M3
+    S.1111.111).  Some rows hold one NaN, one holds NaNs only, and the NaN
+    sits in a lane's first piece, second piece or the 64-wide tail."""
+    import torch
+
+    w = W.mla_workload("gn", 871, [40, 30], [5, 0], num_heads=1, page_size=16,
+                       max_seq_len=128, cache_dtype=cache_dtype)
+    g = W.mla_gather(w, dynamic=True)
+    v = g.cache.view6()
+    nan_code = 0x7FC1 if cache_dtype == W.DTYPE_BF16 else 0x7F
+    rng = np.random.default_rng(872)
+    for b in range(2):
+        for p in range(int(g.ctx_offsets[b + 1] - g.ctx_offsets[b])):
+            page = int(g.cache.page_table[b, p // 16])
+            row = v[page, 0, g.layer_idx, p % 16, 0]
+            if p == 7:
+                row[:] = nan_code
+            elif p % 3 == 1:
+                col = [3, 300, 520, int(rng.integers(0, 576))][p % 4]
+                row[col] = nan_code | (0x8000 if cache_dtype == W.DTYPE_BF16 and p % 2 else 0)
+    d = dev.DeviceGather(g)
+    d.run()
+    torch.cuda.synchronize()
+    ref, ref_scales, f_ref = orc.mla_gather_latent_dynamic(
+        g.cache, g.layer_idx, g.ctx_offsets, out=d.out_init.copy(),
+        scales=np.zeros(g.rows, np.float32))
+    assert d.guards_intact() and d.flags() == f_ref
+    assert np.array_equal(d.scales.host(), ref_scales)
+    got = d.out.host()
+    src = np.stack([v[int(g.cache.page_table[b, p // 16]), 0, g.layer_idx, p % 16, 0]
+                    for b in range(2) for p in range(int(g.ctx_offsets[b + 1] - g.ctx_offsets[b]))])
+    if cache_dtype == W.DTYPE_BF16:
+        is_nan = (src & 0x7FFF) > 0x7F80
+    else:
+        is_nan = (src & 0x7F) == 0x7F
+    assert is_nan.any()
+    assert np.array_equal(got[~is_nan], ref[~is_nan])
+    assert np.all((got[is_nan] & 0x7F) == 0x7F)
+
+
 def test_gather_dynamic_prefill_full(orc, dev):
     run_gather(orc, dev, W.REGISTRY["mla_gather_prefill_dynamic"][0](2))
 
