@@ -221,7 +221,7 @@ __device__ __forceinline__ void unpack8_perm(const uint4& v, float (&f)[8]) {
 }
 
 template <int TL, int VPL, int RPT, bool MBC>
-__global__ void __launch_bounds__(kThreads, 3) rms_norm_rows_kernel(const KnArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) rms_norm_rows_kernel(const KnArgs a) {
     static_assert(RPT <= TL, "a team lane computes the 1/rms of one row of its team");
     constexpr uint32_t kTeams = 32u / TL;
     constexpr uint32_t kRowsWt = kTeams * RPT;  // rows of a warp tile
@@ -377,8 +377,9 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_rows_kernel(const KnArgs
 // `smem` holds the ragged tables; `pt_words` page-table words may be staged
 // behind them (at word a.pt_at).  Staging costs every CTA the copy of the
 // whole table before its first slot resolution and saves a global round trip
-// on each later one, so it is used when warps walk two or more tiles
-// (same-box A/B: 9% faster with about 2.3 tiles per warp, 3% slower with 1.1).
+// on each later one, so it is used when warps walk 1.5 or more tiles on
+// average (same-box A/B: 9% faster with 1.7-2.3 tiles per warp, 3% slower
+// with 1.1).
 template <int TL, int VPL, int RPT, bool MBC>
 cudaError_t launch_rows(const KnArgs& a, size_t smem, uint32_t pt_words, cudaStream_t stream) {
     constexpr auto k = rms_norm_rows_kernel<TL, VPL, RPT, MBC>;
@@ -392,7 +393,7 @@ cudaError_t launch_rows(const KnArgs& a, size_t smem, uint32_t pt_words, cudaStr
     if (wave == 0) return cudaErrorInvalidConfiguration;
     const uint32_t grid = tiles < wave ? tiles : (uint32_t)wave;
     KnArgs b = a;
-    b.pt_words = (uint64_t)wtiles >= 2ull * grid * (kThreads / 32) ? pt_words : 0u;
+    b.pt_words = 2ull * wtiles >= 3ull * grid * (kThreads / 32) ? pt_words : 0u;
     k<<<grid, kThreads, b.pt_words ? smem_pt : smem, stream>>>(b);
     return cudaGetLastError();
 }

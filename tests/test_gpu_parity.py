@@ -392,8 +392,9 @@ def test_knorm_error_flags(orc, dev):
 @pytest.mark.parametrize("G", [128, 64])
 def test_knorm_full_with_bad_pages(orc, dev, G):
     """The benchmark batch with an unmapped page and a page id past the cache.
-    With G = 128 the warps walk more than two tiles each, so the kernel reads
-    the page table from its shared-memory copy; with G = 64 from global."""
+    With G = 128 the warps walk about 1.7 tiles each, so the kernel reads the
+    page table from its shared-memory copy; with G = 64 (one tile per warp)
+    from global memory."""
     w = W.knorm_paged(gamma_len=G)
     c = w.cache
     lens = np.diff(w.offsets.astype(np.int64))
