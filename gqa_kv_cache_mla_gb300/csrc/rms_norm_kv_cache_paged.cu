@@ -8,7 +8,7 @@
 //
 // GB300 design.  A "row" is one (token, kv head) slice of gamma_len leading
 // columns (or the whole K row of a token when per_head_norm is off).  A team
-// of TL lanes (a power of two, 4..32) owns a row: lane l holds 16-byte
+// of TL lanes (a power of two, 2..32) owns a row: lane l holds 16-byte
 // vectors l, l + TL, ... of it, sums its squares, and an xor-shuffle inside
 // the team finishes the reduction, so no shared memory or block barrier is
 // needed for the norm itself.  Each team handles RPT rows so every thread has
@@ -20,6 +20,11 @@
 // shared memory while the current tile's loads are in flight, then
 // normalises the tile and writes it back in place.  Columns at or past
 // gamma_len are neither read into the sum nor written.
+// Two kernels share this design: rms_norm_rows_kernel, for rows whose
+// normalised columns are contiguous and a multiple of 8 wide (per-head
+// norms, whole rows of adjacent heads), with the team geometry fixed at
+// compile time; and rms_norm_kv_kernel for everything else (ragged gamma
+// lengths, whole rows of padded heads), with run-time geometry.
 #include <cstdint>
 
 #include "kvw_device.cuh"
@@ -30,7 +35,6 @@ namespace {
 constexpr uint32_t kThreads = 256;
 constexpr uint32_t kMaxCols = 2048;
 constexpr uint32_t kMaxWarpTileTokens = 66;  // tokens of a warp tile: up to 64 rows + 2
-
 
 struct KnArgs {
     uint16_t* cache;
@@ -193,19 +197,6 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
     }
 }
 
-// Fast path for contiguous rows: the normalised columns of a row are adjacent
-// in memory (per-head norm, or the whole K row of a token whose heads are
-// adjacent) and gamma_len is a multiple of 8.  The team geometry (TL lanes,
-// VPL 16-byte vectors per lane, RPT rows per team) is compile-time, so lane
-// tl of a team owns columns 8 (tl + v TL) .. + 7 of every row of the launch:
-// a row is one base pointer plus constant offsets and the team reduction
-// unrolls.  The sum of squares runs as VPL independent fused multiply-add
-// chains; team lane q computes the 1/rms of row q of its team (rsqrt refined
-// by one Newton-Raphson step, r' = r (3 - m r^2) / 2, within two fp32 ulp of
-// the correctly rounded value, so a bf16 result differs from a correctly
-// rounded reference by at most one ulp, on a few elements in 10^5) and the
-// team reads the values back with shuffles.  Slot resolution, tiling and the
-// per-warp walk are those of rms_norm_kv_kernel.
 // Exact bf16 widening by byte permutes: the same values as unpack8, from a
 // different instruction sequence.  The sum-of-squares pass uses this one and
 // the output pass unpack8, so the compiler re-widens the packed rows for the
@@ -220,6 +211,20 @@ __device__ __forceinline__ void unpack8_perm(const uint4& v, float (&f)[8]) {
     }
 }
 
+// Fast path for contiguous rows: the normalised columns of a row are adjacent
+// in memory (per-head norm, or the whole K row of a token whose heads are
+// adjacent) and gamma_len is a multiple of 8.  The team geometry (TL lanes,
+// VPL 16-byte vectors per lane, RPT rows per team) is compile-time, so lane
+// tl of a team owns columns 8 (tl + v TL) .. + 7 of every row of the launch:
+// a row is one base pointer plus constant offsets and the team reduction
+// unrolls.  The sum of squares runs as VPL independent fused multiply-add
+// chains; team lane q computes the 1/rms of row q of its team (rsqrt refined
+// by one Newton-Raphson step, r' = r (3 - m r^2) / 2, within two fp32 ulp of
+// the correctly rounded value, so a bf16 result differs from a correctly
+// rounded reference by at most one ulp, on a few elements in 10^5) and the
+// team reads the values back with shuffles.  Slot resolution, tiling and the
+// per-warp walk are those of rms_norm_kv_kernel; a small page table can be
+// staged in shared memory with the ragged tables (see launch_rows).
 template <int TL, int VPL, int RPT, bool MBC>
 __global__ void __launch_bounds__(kThreads, 4) rms_norm_rows_kernel(const KnArgs a) {
     static_assert(RPT <= TL, "a team lane computes the 1/rms of one row of its team");
