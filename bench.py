@@ -414,12 +414,13 @@ def measure(name, steps, warmup, dev, rank, world, flusher, e2e=True, cpu_s=None
                     "ms_per_step": r["ms"],
                     "copy_floor_ms": floor["both_ms"], "e2e_over_copy_floor":
                         r["ms"] / floor["both_ms"] if floor["both_ms"] else None,
-                    "copy_floor": floor,
+                    "copy_floor": floor, "replay_ms_per_step": r["replay_ms_per_step"],
                     "how": "every step: one copy of its packed inputs (and a zeroed error "
                            "word) from pinned host memory, the kvw call, one copy of the "
                            "error word and the outputs back to pinned host memory; steps "
                            "pipelined %d deep on copy-in / compute / copy-out streams, %d "
-                           "steps per CUDA graph replay" % (r["depth"], r["per_graph"])}
+                           "steps per CUDA graph replay, mean over %d replays" % (
+                               r["depth"], r["per_graph"], len(r["replay_ms_per_step"]))}
 
     peak, peak_src = measured_peak()
     achieved = abytes / (ms / 1000.0) / 1e9
@@ -725,17 +726,20 @@ def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=3, per_graph=32, chun
             done = torch.cuda.Event()
             done.record(st)
             cap.wait_event(done)
-    reps = max(1, (steps + K - 1) // K)
+    # at least three replays, each timed on its own (the host link is shared
+    # with other work on the node: one replay alone can catch a slow moment)
+    reps = max(3, (steps + K - 1) // K)
     for _ in range(max(1, warmup // K)):
         graph.replay()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launch = torch.cuda.current_stream(dev)
-    a.record(launch)
-    for _ in range(reps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(launch)
+    for i in range(reps):
         graph.replay()
-    b.record(launch)
+        ev[i + 1].record(launch)
     torch.cuda.synchronize()
+    replay_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
     for S in sets:
         assert int(S["h_out"][:4].view(torch.int32)[0]) == 0, "data errors in the e2e run"
     if outs:  # the results read back equal the device path's results
@@ -744,9 +748,9 @@ def measure_e2e(d, w, k, stream, dev, steps, warmup, depth=3, per_graph=32, chun
         n = t.numel() * t.element_size()
         assert torch.equal(sets[0]["h_out"][o:o + n], t.reshape(-1).view(torch.uint8).cpu()), \
             "e2e results differ from the device run"
-    steps = reps * K
-    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h, "depth": depth,
-            "per_graph": K, "chunks": chunks}
+    return {"ms": sum(replay_ms) / (reps * K), "h2d": h2d, "d2h": d2h, "depth": depth,
+            "per_graph": K, "chunks": chunks,
+            "replay_ms_per_step": [round(t / K, 4) for t in replay_ms]}
 
 
 def main():
