@@ -147,6 +147,34 @@ __device__ __forceinline__ float div_refined(float x, float s, float y) {
 
 __device__ __forceinline__ bool refined_ok(float sc) { return sc >= 0x1p-60f && sc <= 0x1p60f; }
 
+// Unsigned 32-bit division by a run-time invariant d >= 1 as a multiply-high,
+// an add and a shift (T. Granlund and P. L. Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, section 4): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1 (m < 2^32),
+// floor(n / d) = (umulhi(m, n) + n) >> l for every 32-bit n, the sum taken
+// in 64 bits.  The host computes (m, l) once per launch (make_fast_div).
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+inline FastDiv make_fast_div(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((1ull << f.l) < d) ++f.l;
+    f.m = (uint32_t)(((((uint64_t)1 << f.l) - d) << 32) / d + 1);
+    return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+    const uint32_t hi = __umulhi(f.m, n);
+#else
+    const uint32_t hi = (uint32_t)(((uint64_t)f.m * n) >> 32);
+#endif
+    return (uint32_t)(((uint64_t)hi + n) >> f.l);
+}
+
 __device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
     if (err_flags) atomicOr(err_flags, bits);
 }

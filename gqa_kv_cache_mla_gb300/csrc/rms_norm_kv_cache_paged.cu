@@ -54,6 +54,8 @@ struct KnArgs {
     float inv_g;              // 1 / gamma_len (rounded)
     uint32_t pt_words;        // page-table words staged in shared memory (0: read from global)
     uint32_t pt_at;           // their word offset in dynamic shared memory
+    FastDiv rpt_div;          // division by rows_per_token
+    FastDiv ps_div;           // division by page_size
     int mbc;
 };
 
@@ -95,8 +97,8 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
     int64_t* wbase = s_wbase[warp];
     auto resolve = [&](uint32_t wt) {
         const uint32_t r0 = wt * rows_wt;
-        const uint32_t t_lo = r0 / a.rows_per_token;
-        const uint32_t t_hi = (min(r0 + rows_wt, a.rows) - 1) / a.rows_per_token;
+        const uint32_t t_lo = fast_div(r0, a.rpt_div);
+        const uint32_t t_hi = fast_div(min(r0 + rows_wt, a.rows) - 1, a.rpt_div);
         for (uint32_t k = lane; k <= t_hi - t_lo; k += 32) {
             const uint32_t t = t_lo + k;
             const uint32_t b = find_request(s_off, a.B, t);
@@ -113,16 +115,16 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
 
     for (; wt < wtiles; wt += nwarps) {
     const uint32_t r0 = wt * rows_wt;
-    const uint32_t t_lo = r0 / a.rows_per_token;
+    const uint32_t t_lo = fast_div(r0, a.rpt_div);
     const uint32_t r_end = min(r0 + rows_wt, a.rows);
 
     // pointers of this lane's first vector in each of its rows (null: no row);
     // row r = r0 + team + q * teams, walked as (token, head) without dividing
     uint16_t* ptr[RPT];
     uint4 x[RPT][VPL];
-    uint32_t t = (r0 + team) / a.rows_per_token;
+    uint32_t t = fast_div(r0 + team, a.rpt_div);
     uint32_t g = (r0 + team) - t * a.rows_per_token;
-    const uint32_t dt = teams / a.rows_per_token, dg = teams - dt * a.rows_per_token;
+    const uint32_t dt = fast_div(teams, a.rpt_div), dg = teams - dt * a.rows_per_token;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
         const uint32_t r = r0 + team + q * teams;
@@ -260,27 +262,26 @@ __global__ void __launch_bounds__(kThreads, 4) rms_norm_rows_kernel(const KnArgs
     const uint32_t wtiles = (a.rows + kRowsWt - 1) / kRowsWt;
     const uint32_t nwarps = gridDim.x * (kThreads / 32);
     int64_t* wbase = s_wbase[warp];
+    // divisions by rows_per_token and page_size are multiply-highs (FastDiv)
     auto resolve = [&](uint32_t wt) {
         const uint32_t r0 = wt * kRowsWt;
-        const uint32_t t_lo = r0 / a.rows_per_token;
-        const uint32_t t_hi = (min(r0 + kRowsWt, a.rows) - 1) / a.rows_per_token;
+        const uint32_t t_lo = fast_div(r0, a.rpt_div);
+        const uint32_t t_hi = fast_div(min(r0 + kRowsWt, a.rows) - 1, a.rpt_div);
         for (uint32_t k = lane; k <= t_hi - t_lo; k += 32) {
             const uint32_t t = t_lo + k;
             const uint32_t b = find_request(s_off, a.B, t);
             const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-            int64_t base;
-            if (a.pt_words) {
-                base = -1;
-                const uint32_t pidx = (uint32_t)(pos / a.page_size);
-                if ((pos >> 32) == 0 && pidx < a.max_pages) {
-                    const uint32_t page = s_pt[b * a.max_pages + pidx];
+            int64_t base = -1;
+            if ((pos >> 32) == 0) {  // no page table reaches past 32-bit positions
+                const uint32_t p32 = (uint32_t)pos;
+                const uint32_t pidx = fast_div(p32, a.ps_div);
+                if (pidx < a.max_pages) {
+                    const uint32_t page = a.pt_words ? s_pt[b * a.max_pages + pidx]
+                                                     : __ldg(a.page_table + (uint64_t)b * a.max_pages + pidx);
                     if (page < a.num_pages)
                         base = (int64_t)page * a.s_page + a.layer_off +
-                               (int64_t)((uint32_t)pos - pidx * a.page_size) * a.s_token;
+                               (int64_t)(p32 - pidx * a.page_size) * a.s_token;
                 }
-            } else {
-                base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
-                                a.s_token, a.layer_off, b, pos);
             }
             wbase[k] = base;
             if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
@@ -293,14 +294,14 @@ __global__ void __launch_bounds__(kThreads, 4) rms_norm_rows_kernel(const KnArgs
     const uint32_t nvec = a.nv;
     for (; wt < wtiles; wt += nwarps) {
         const uint32_t r0 = wt * kRowsWt;
-        const uint32_t t_lo = r0 / a.rows_per_token;
+        const uint32_t t_lo = fast_div(r0, a.rpt_div);
         const uint32_t r_end = min(r0 + kRowsWt, a.rows);
         // row r = r0 + team + q * kTeams, walked as (token, head) without dividing
         uint16_t* ptr[RPT];
         uint4 x[RPT][VPL];
-        uint32_t t = (r0 + team) / a.rows_per_token;
+        uint32_t t = fast_div(r0 + team, a.rpt_div);
         uint32_t g = (r0 + team) - t * a.rows_per_token;
-        const uint32_t dt = kTeams / a.rows_per_token, dg = kTeams - dt * a.rows_per_token;
+        const uint32_t dt = fast_div(kTeams, a.rpt_div), dg = kTeams - dt * a.rows_per_token;
 #pragma unroll
         for (int q = 0; q < RPT; ++q) {
             const uint32_t r = r0 + team + q * kTeams;
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 4) rms_norm_rows_kernel(const KnArgs
             for (int o = TL / 2; o > 0; o >>= 1)
                 ss[q] = __fadd_rn(ss[q], __shfl_xor_sync(0xffffffffu, ss[q], o));
         }
-        // one correctly rounded 1/rms per row: team lane q computes row q's
+        // one 1/rms per row: team lane q computes row q's
         // and the team reads them back, instead of every lane computing all
         float mine = ss[0];
 #pragma unroll
@@ -493,6 +494,8 @@ extern "C" int kvw_rms_norm_kv_cache_paged(const kvw_paged_cache_t* cache, const
     a.page_size = cache->page_size;
     a.per_head = per_head_norm ? 1u : 0u;
     a.rows_per_token = per_head_norm ? cache->num_heads : 1u;
+    a.rpt_div = make_fast_div(a.rows_per_token);
+    a.ps_div = make_fast_div(cache->page_size);
     a.nv = (gamma_len + 7) / 8;
     // Team of TL lanes per row, each lane VPL 16-byte vectors: narrow teams
     // (4 lanes for up to 16 vectors) let one instruction stream serve many
