@@ -147,6 +147,10 @@ __device__ __forceinline__ float div_refined(float x, float s, float y) {
 
 __device__ __forceinline__ bool refined_ok(float sc) { return sc >= 0x1p-60f && sc <= 0x1p60f; }
 
+__device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
+    if (err_flags) atomicOr(err_flags, bits);
+}
+
 // Unsigned 32-bit division by a run-time invariant d >= 1 as a multiply-high,
 // an add and a shift (T. Granlund and P. L. Montgomery, "Division by
 // invariant integers using multiplication", PLDI 1994, section 4): with
@@ -173,10 +177,6 @@ __host__ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv&
     const uint32_t hi = (uint32_t)(((uint64_t)f.m * n) >> 32);
 #endif
     return (uint32_t)(((uint64_t)hi + n) >> f.l);
-}
-
-__device__ __forceinline__ void flag(uint32_t* err_flags, uint32_t bits) {
-    if (err_flags) atomicOr(err_flags, bits);
 }
 
 // ------------------------------------------------------------ ragged lookup
@@ -272,14 +272,14 @@ __device__ __forceinline__ uint32_t page_of(const uint32_t* __restrict__ page_ta
 }
 
 // Element offset of the K row of slot `pos` of request b in `layer_off`, or
-// -1 when the slot maps to no valid page.
+// -1 when the slot maps to no valid page.  `ps` divides by the page size.
 __device__ __forceinline__ int64_t slot_row(const uint32_t* __restrict__ page_table,
                                            uint32_t max_pages, uint32_t num_pages,
-                                           uint32_t page_size, int64_t s_page, int64_t s_token,
+                                           const FastDiv& ps, int64_t s_page, int64_t s_token,
                                            int64_t layer_off, uint32_t b, uint64_t pos) {
     if (pos >> 32) return -1;  // no page table reaches that far (max_pages is 32-bit)
     const uint32_t p32 = (uint32_t)pos;
-    const uint32_t pidx = p32 / page_size, row = p32 - pidx * page_size;
+    const uint32_t pidx = fast_div(p32, ps), row = p32 - pidx * ps.d;
     if (pidx >= max_pages) return -1;
     const uint32_t page = __ldg(page_table + (uint64_t)b * max_pages + pidx);
     if (page >= num_pages) return -1;

@@ -39,6 +39,7 @@ struct GatherArgs {
     int64_t s_page, s_token, layer_off;  // cache elements
     uint32_t B, rows, max_pages, num_pages, page_size;
     float cache_scale, out_scale;
+    FastDiv ps_div;  // division by page_size
 };
 
 // Raw bytes of 8 cache elements at element offset `e` (16 bytes of bf16 or
@@ -72,7 +73,7 @@ __device__ __forceinline__ int64_t row_base(const GatherArgs& a, const uint32_t*
     if (r >= a.rows) return -1;
     const uint32_t b = find_request(s_off, a.B, r);
     const uint32_t pos = r - s_off[b];
-    const uint32_t pidx = pos / a.page_size;
+    const uint32_t pidx = fast_div(pos, a.ps_div);
     const uint32_t page = pidx < a.max_pages
                               ? __ldg(a.page_table + (uint64_t)b * a.max_pages + pidx)
                               : KVW_PAGE_UNMAPPED;
@@ -408,6 +409,7 @@ int make_args(const kvw_paged_cache_t* cache, uint32_t layer_idx, const uint32_t
     a.max_pages = cache->max_pages_per_seq;
     a.num_pages = cache->num_pages;
     a.page_size = cache->page_size;
+    a.ps_div = make_fast_div(cache->page_size);
     a.cache_scale = cache->scale;
     a.out_scale = 1.0f;
     return KVW_OK;

@@ -61,6 +61,8 @@ struct MlaArgs {
     uint32_t kv_blocks;
     uint32_t decode;  // T == B: try the one-token-per-request fast path first
     float eps, scale;
+    FastDiv ps_div;   // division by page_size
+    FastDiv vpt_div;  // division by the 16-byte q vectors per token (H * 8)
 };
 
 // Stage offsets[0..B] and cache_lengths[0..B-1] in shared memory and check
@@ -184,7 +186,7 @@ __device__ __forceinline__ void latent_rows(const MlaArgs& a, uint32_t* s_off, u
         if (lane == 0) flag(a.err_flags, KVW_ERR_POSITION);
         return;
     }
-    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+    const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.ps_div, a.s_page,
                                   a.s_token, a.layer_off, b, pos);
     if (base < 0) {
         if (lane == 0) flag(a.err_flags, KVW_ERR_PAGE);
@@ -222,7 +224,7 @@ __device__ __forceinline__ bool latent_rows_decode(const MlaArgs& a) {
     uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, xr = x0, g0 = x0, g1 = x0;
     if (active) latent_row_loads<INPLACE>(a, t, lane, x0, x1, xr, g0, g1);
     const bool pos_ok = pos < a.freqs_rows;
-    const uint32_t pidx = pos / a.page_size;
+    const uint32_t pidx = fast_div(pos, a.ps_div);
     uint32_t page = KVW_PAGE_UNMAPPED;
     float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa;
     if (active && pos_ok) {
@@ -279,7 +281,7 @@ __device__ __forceinline__ bool q_rows_decode(const MlaArgs& a) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const uint32_t v = vbase + threadIdx.x + i * kThreads;
-        pos[i] = v < a.q_vectors ? __ldg(a.cache_lengths + v / vpt) : 0xffffffffu;
+        pos[i] = v < a.q_vectors ? __ldg(a.cache_lengths + fast_div(v, a.vpt_div)) : 0xffffffffu;
     }
     uint4 x[VPT];
 #pragma unroll
@@ -334,9 +336,9 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
         return;
     }
     const uint32_t vpt = a.H * 8u;  // vectors per token
-    const uint32_t t0 = vbase / vpt;
+    const uint32_t t0 = fast_div(vbase, a.vpt_div);
     const uint32_t vlast = min(vbase + kThreads * VPT, a.q_vectors) - 1u;
-    const uint32_t ntok = vlast / vpt - t0 + 1u;
+    const uint32_t ntok = fast_div(vlast, a.vpt_div) - t0 + 1u;
     for (uint32_t k = threadIdx.x; k < ntok; k += kThreads) {
         const uint32_t t = t0 + k;
         const uint32_t b = find_request(s_off, a.B, t);
@@ -356,7 +358,7 @@ __device__ __forceinline__ void q_rows(const MlaArgs& a, uint32_t* s_off, uint32
     for (int i = 0; i < VPT; ++i) {
         const uint32_t v = vbase + threadIdx.x + i * kThreads;
         if (v >= a.q_vectors) break;
-        const uint32_t t = v / vpt;
+        const uint32_t t = fast_div(v, a.vpt_div);
         if (t != cur_t) {
             cur_t = t;
             p = s_pos[t - t0];
@@ -515,6 +517,8 @@ int mla_entry(void* q_rope_out, int32_t out_dtype, const void* q_rope,
     a.page_size = cache->page_size;
     a.kv_blocks = (tot_seq_len + kRowsPerKvBlock - 1) / kRowsPerKvBlock;
     a.decode = tot_seq_len == num_batches ? 1u : 0u;
+    a.ps_div = make_fast_div(cache->page_size);
+    a.vpt_div = make_fast_div(num_heads > 0 ? num_heads * 8u : 1u);
     a.eps = epsilon;
     a.scale = cache->scale;
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)num_batches + 1);

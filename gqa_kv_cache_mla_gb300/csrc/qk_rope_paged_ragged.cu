@@ -73,6 +73,9 @@ struct GqaArgs {
     uint32_t slices;            // head slices per (token, pair group)
     uint32_t items;             // (Hq + Hk) * S / 16 (register-staged kernel)
     uint64_t wait_ns;           // limit of every mbarrier wait of the pipeline
+    FastDiv ps_div;             // division by page_size
+    FastDiv g_div, sl_div;      // by the 8-pair groups per head and the head slices
+    FastDiv half_div;           // by the pairs per head (S / 2)
 };
 
 __device__ __forceinline__ uint32_t section_of(const GqaArgs& a, uint32_t k) {
@@ -127,7 +130,7 @@ __device__ __forceinline__ void producer(const GqaArgs& a, uint64_t* full, uint6
             if (!qok) {
                 flag(a.err_flags, KVW_ERR_POSITION);
             } else {
-                kbase = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+                kbase = slot_row(a.page_table, a.max_pages, a.num_pages, a.ps_div, a.s_page,
                                  a.s_token, a.layer_off, b, pos);
                 if (kbase < 0) flag(a.err_flags, KVW_ERR_PAGE);
                 bytes += a.S * 4u;  // the freqs row
@@ -226,10 +229,10 @@ __device__ __forceinline__ void consumer(const GqaArgs& a, uint64_t* full, uint6
         const uint32_t t0 = g * a.tpb;
         const uint32_t ntok = min(a.tpb, a.T - t0);
         for (uint32_t w = tid; w < units; w += kConsumers) {
-            const uint32_t m = w % G;
-            const uint32_t rest = w / G;
-            const uint32_t sl = rest % a.slices;
-            const uint32_t u = rest / a.slices;
+            const uint32_t rest = fast_div(w, a.g_div);
+            const uint32_t m = w - rest * G;
+            const uint32_t u = fast_div(rest, a.sl_div);
+            const uint32_t sl = rest - u * a.slices;
             if (u >= ntok) continue;
             const TokMeta tm = meta[u];
             if (!tm.qok) continue;
@@ -419,7 +422,7 @@ __device__ __forceinline__ void staged_prepare(const GqaArgs& a, const uint32_t*
         if (t < a.T) {
             const uint32_t b = find_request(s_off, a.B, t);
             const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-            base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size, a.s_page,
+            base = slot_row(a.page_table, a.max_pages, a.num_pages, a.ps_div, a.s_page,
                             a.s_token, a.layer_off, b, pos);
             if (a.mode == 0) {
                 bad = pos >= a.freqs_rows;
@@ -437,7 +440,7 @@ __device__ __forceinline__ void staged_prepare(const GqaArgs& a, const uint32_t*
     }
     const uint32_t half = a.S >> 1;
     for (uint32_t idx = threadIdx.x; idx < TPB * half; idx += blockDim.x) {
-        const uint32_t u = idx / half, k = idx % half;
+        const uint32_t u = fast_div(idx, a.half_div), k = idx - u * half;
         const uint32_t t = t_begin + u;
         if (t >= a.T) continue;
         uint64_t p;
@@ -667,6 +670,10 @@ int qk_entry(const void* q_proj, const uint32_t* input_row_offsets, uint32_t num
     a.sec01 = sec01;
     a.items = (uint32_t)items;
     a.wait_ns = wait_ns;
+    a.ps_div = make_fast_div(cache->page_size);
+    a.half_div = make_fast_div(S / 2);
+    a.g_div = make_fast_div(S / 16);
+    a.sl_div = make_fast_div(1);
     if (withhold && a.mode == 2) return KVW_EUNSUPPORTED;  // the hook is in the pipeline only
     if (a.mode == 2) {
         const uint32_t threads = (uint32_t)((items + 31) / 32 * 32);
@@ -750,6 +757,7 @@ int qk_entry(const void* q_proj, const uint32_t* input_row_offsets, uint32_t num
     a.slices = (uint32_t)(kConsumers / (tpb * G));
     if (a.slices < 1) a.slices = 1;
     if (a.slices > num_q_heads + a.Hk) a.slices = num_q_heads + a.Hk;
+    a.sl_div = make_fast_div(a.slices);
     const size_t smem = 128 + (size_t)tables + (size_t)kStages * a.stage_bytes;
     if (smem > (size_t)optin) return KVW_EUNSUPPORTED;
     cudaError_t e;

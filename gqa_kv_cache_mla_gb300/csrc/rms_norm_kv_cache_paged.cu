@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 3) rms_norm_kv_kernel(const KnArgs a
             const uint32_t t = t_lo + k;
             const uint32_t b = find_request(s_off, a.B, t);
             const uint64_t pos = (uint64_t)s_clen[b] + (t - s_off[b]);
-            const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.page_size,
+            const int64_t base = slot_row(a.page_table, a.max_pages, a.num_pages, a.ps_div,
                                           a.s_page, a.s_token, a.layer_off, b, pos);
             wbase[k] = base;
             if (base < 0) flag(a.err_flags, KVW_ERR_PAGE);
