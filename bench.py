@@ -8,8 +8,9 @@ the MLA write.  A step is one call of ``kvw_mla_rope_rmsnorm_quant`` over that
 batch: RoPE on q_rope and on the rope part, RMSNorm of the latent part, FP8
 quantisation and the paged scatter.  The same run then measures, under the
 line's ``also`` key, the MLA decode step (256 requests x 1 token, with its
-end-to-end figure), the bf16-cache prefill, the GQA Q/K RoPE and the K-cache
-RMSNorm launches the same way.  ``--workload`` picks another main workload.
+end-to-end figure), the bf16-cache prefill, the GQA Q/K RoPE (bf16 and E4M3
+K cache), the K-cache RMSNorm and the latent gather with dynamic FP8
+launches the same way.  ``--workload`` picks another main workload.
 
 Timing: W warm-up steps, then K timed steps between a barrier and a device
 synchronize on both sides.  Each step's launch is bracketed by CUDA events on
@@ -49,7 +50,8 @@ WORKLOADS = W.REGISTRY
 DEFAULT_SEED = 2
 DEFAULT_WORKLOAD = "mla_prefill_fp8"
 # measured after the main workload, in the same run, under the line's "also" key
-DEFAULT_ALSO = ("mla_decode", "mla_prefill_bf16", "gqa_interleaved", "knorm128", "knorm64")
+DEFAULT_ALSO = ("mla_decode", "mla_prefill_bf16", "gqa_interleaved", "gqa_fp8k", "knorm128",
+                "knorm64", "mla_gather_prefill_dynamic")
 HEADLINE = ("mla_prefill_fp8", "mla_prefill_bf16", "mla_decode", "mla_decode_bf16")
 
 

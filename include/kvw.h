@@ -300,6 +300,12 @@ int kvw_qk_rope_paged_ragged(const void* q_proj, const uint32_t* input_row_offse
  * computed in fp32 and rounded once to bf16 (multiply_before_cast != 0), or
  * with the normalised value rounded to bf16 before the multiply
  * (multiply_before_cast == 0).  Columns >= gamma_len are not touched.
+ * The sum of squares is accumulated in an order of the kernel's choosing
+ * and, for 8-aligned gamma lengths of contiguous rows, the 1/rms factor is
+ * an rsqrt estimate refined by one Newton-Raphson step (within two fp32 ulp
+ * of the correctly rounded value): results are within one bf16 ulp of a
+ * correctly rounded evaluation of the formula (two roundings' worth with
+ * multiply_before_cast == 0).
  * With per_head_norm == 0 the whole K row of the token (num_heads *
  * head_size values) is normalised as one vector and gamma_len must equal
  * that width.
