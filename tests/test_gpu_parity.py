@@ -678,6 +678,52 @@ def test_gather_dynamic_nan_values(orc, dev, cache_dtype):
     assert np.all((got[is_nan] & 0x7F) == 0x7F)
 
 
+def test_gather_dynamic_every_bf16_maximum(orc, dev):
+    """Row r's largest magnitude is the bf16 pattern min(r, 0x7F80), from 0 and
+    the subnormals through every binade to infinity, at column r % 576 with
+    either sign; the other values are random patterns below it.  Scales
+    (amax / 448) and codes bit for bit, so every row maximum takes the
+    scale path the kernel gives it: the refined division by 448 in the normal
+    range, the IEEE divide at both ends, and the IEEE divide of the values
+    where the scale leaves the refined range."""
+    n = 0x7F80 + 4
+    w = W.mla_workload("gm", 880, [1, 1, 1, 1], [8200, 8200, 8200, n - 4 * 8201 + 8200],
+                       num_heads=1, page_size=64, max_seq_len=8256, cache_dtype=W.DTYPE_BF16)
+    g = W.mla_gather(w, dynamic=True)
+    assert int(g.ctx_offsets[-1]) == n
+    rng = np.random.default_rng(881)
+    top = np.minimum(np.arange(n), 0x7F80).astype(np.int64)
+    rows = (rng.random((n, 576)) * (top[:, None] + 1)).astype(np.int64)
+    rows = np.minimum(rows, top[:, None])
+    rows[np.arange(n), np.arange(n) % 576] = top
+    rows |= rng.integers(0, 2, size=rows.shape) << 15
+    rows = rows.astype(np.uint16)
+    v = g.cache.view6()
+    P = g.cache.page_size
+    for b in range(4):
+        lo, hi = int(g.ctx_offsets[b]), int(g.ctx_offsets[b + 1])
+        p = np.arange(hi - lo)
+        v[g.cache.page_table[b, p // P].astype(np.int64), 0, g.layer_idx, p % P, 0] = rows[lo:hi]
+    import torch
+
+    d = dev.DeviceGather(g)
+    d.run()
+    torch.cuda.synchronize()
+    ref, ref_scales, f_ref = orc.mla_gather_latent_dynamic(
+        g.cache, g.layer_idx, g.ctx_offsets, out=d.out_init.copy(),
+        scales=np.zeros(g.rows, np.float32))
+    assert d.guards_intact() and d.flags() == f_ref
+    assert np.array_equal(d.scales.host(), ref_scales)
+    got = d.out.host()
+    # An infinite value in a row whose scale is infinite gives inf / inf, a NaN
+    # whose sign IEEE 754 leaves open (the host's division picks one by
+    # platform): NaN codes compare up to the sign, every other code exactly.
+    is_nan = (ref & 0x7F) == 0x7F
+    assert is_nan.sum() == np.count_nonzero((rows & 0x7FFF) == 0x7F80)
+    assert np.array_equal(got[~is_nan], ref[~is_nan])
+    assert np.all((got[is_nan] & 0x7F) == 0x7F)
+
+
 def test_gather_dynamic_prefill_full(orc, dev):
     run_gather(orc, dev, W.REGISTRY["mla_gather_prefill_dynamic"][0](2))
 
