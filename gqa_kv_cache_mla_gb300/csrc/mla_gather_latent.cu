@@ -39,7 +39,8 @@ struct GatherArgs {
     int64_t s_page, s_token, layer_off;  // cache elements
     uint32_t B, rows, max_pages, num_pages, page_size;
     float cache_scale, out_scale;
-    FastDiv ps_div;  // division by page_size
+    FastDiv ps_div;    // division by page_size
+    uint64_t wait_ns;  // limit of every mbarrier wait
 };
 
 // Raw bytes of 8 cache elements at element offset `e` (16 bytes of bf16 or
@@ -311,7 +312,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <bool CF8>
+// WITHHOLD (test builds only): the first step of every warp is announced on
+// its stage barrier but not copied, so the warp's wait for it runs into its
+// limit.
+template <bool CF8, bool WITHHOLD = false>
 __global__ void __launch_bounds__(kDynThreads, kDynCtasPerSm)
     gather_dynamic_kernel(const GatherArgs a, float* scales) {
     constexpr uint32_t S = kDynStages<CF8>, RB = kDynRowBytes<CF8>, SB = kDynStageBytes<CF8>;
@@ -344,11 +348,11 @@ __global__ void __launch_bounds__(kDynThreads, kDynCtasPerSm)
     const int64_t esz = CF8 ? 1 : 2;
     // Copy the rows of one step (lane q < kDynRows: row q at cache element
     // `base`, or none when base < 0) into stage s; returns the rows copied.
-    auto issue = [&](uint32_t s, int64_t base) -> uint32_t {
+    auto issue = [&](uint32_t s, int64_t base, bool withhold = false) -> uint32_t {
         const uint32_t valid = __ballot_sync(0xffffffffu, lane < kDynRows && base >= 0);
         if (lane == 0) mbar_arrive_expect_tx(&bars[s], __popc(valid) * RB);
         __syncwarp();
-        if ((valid >> lane) & 1u)
+        if (((valid >> lane) & 1u) && !withhold)
             bulk_load(stages + (size_t)s * SB + lane * RB, a.cache + base * esz, RB, &bars[s]);
         return valid;
     };
@@ -363,7 +367,8 @@ __global__ void __launch_bounds__(kDynThreads, kDynCtasPerSm)
         }
 #pragma unroll
         for (uint32_t k = 0; k < S; ++k)
-            if (st0 + k * nwarps < steps) vmask |= issue(k, row_resolve(a, l[k])) << (kDynRows * k);
+            if (st0 + k * nwarps < steps)
+                vmask |= issue(k, row_resolve(a, l[k]), WITHHOLD && k == 0) << (kDynRows * k);
         ahead = l[S];
     }
     const bool bf16_values = !CF8 || a.cache_scale == 1.0f;
@@ -378,11 +383,11 @@ __global__ void __launch_bounds__(kDynThreads, kDynCtasPerSm)
         const RowLookup look_n = ahead;
         const uint32_t nxt2 = nxt + nwarps;
         ahead = row_lookup(a, s_off, lane < kDynRows && nxt2 < steps ? nxt2 * kDynRows + lane : a.rows);
-        if (!mbar_wait(&bars[s], (i / S) & 1u, kWaitLimitNs)) {
+        if (!mbar_wait(&bars[s], (i / S) & 1u, a.wait_ns)) {
             if (lane == 0) flag(a.err_flags, KVW_ERR_TIMEOUT);
             // leave no copy in flight: wait (bounded) for the stages issued after this one
             for (uint32_t k = 1; k < S && st + k * nwarps < steps; ++k)
-                mbar_wait(&bars[(i + k) % S], ((i + k) / S) & 1u, kWaitLimitNs);
+                mbar_wait(&bars[(i + k) % S], ((i + k) / S) & 1u, a.wait_ns);
             return;
         }
         const uint32_t valid = (vmask >> (kDynRows * s)) & ((1u << kDynRows) - 1u);
@@ -506,9 +511,9 @@ cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <bool CF8>
+template <bool CF8, bool WITHHOLD = false>
 cudaError_t launch_dynamic(const GatherArgs& a, float* scales, cudaStream_t stream) {
-    constexpr auto k = gather_dynamic_kernel<CF8>;
+    constexpr auto k = gather_dynamic_kernel<CF8, WITHHOLD>;
     const size_t smem = dyn_smem<CF8>(a.B);
     uint64_t wave = 0;
     const cudaError_t e = wave_ctas<k>(kDynThreads, smem, wave);
@@ -551,6 +556,7 @@ int make_args(const kvw_paged_cache_t* cache, uint32_t layer_idx, const uint32_t
     a.num_pages = cache->num_pages;
     a.page_size = cache->page_size;
     a.ps_div = make_fast_div(cache->page_size);
+    a.wait_ns = kWaitLimitNs;
     a.cache_scale = cache->scale;
     a.out_scale = 1.0f;
     return KVW_OK;
@@ -581,12 +587,13 @@ extern "C" int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_sca
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }
 
-extern "C" int kvw_mla_gather_latent_fp8_dynamic(void* out_codes, float* out_scales,
-                                                 const kvw_paged_cache_t* cache,
-                                                 uint32_t layer_idx, const uint32_t* ctx_offsets,
-                                                 uint32_t num_batches, uint32_t total_rows,
-                                                 uint32_t* err_flags, cudaStream_t stream) {
-    using namespace kvw;
+namespace kvw {
+namespace {
+
+int gather_dynamic_entry(void* out_codes, float* out_scales, const kvw_paged_cache_t* cache,
+                         uint32_t layer_idx, const uint32_t* ctx_offsets, uint32_t num_batches,
+                         uint32_t total_rows, uint32_t* err_flags, cudaStream_t stream,
+                         bool withhold, uint64_t wait_ns) {
     if (!cache) return KVW_EINVAL;
     GatherArgs a;
     const int st = make_args(cache, layer_idx, ctx_offsets, num_batches, total_rows, err_flags, a);
@@ -596,8 +603,49 @@ extern "C" int kvw_mla_gather_latent_fp8_dynamic(void* out_codes, float* out_sca
         (reinterpret_cast<uintptr_t>(out_scales) & 3u) != 0)
         return KVW_EINVAL;
     a.out = static_cast<unsigned char*>(out_codes);
-    const cudaError_t e = cache->dtype == KVW_DTYPE_FP8_E4M3
-                              ? launch_dynamic<true>(a, out_scales, stream)
-                              : launch_dynamic<false>(a, out_scales, stream);
+    a.wait_ns = wait_ns;
+    const bool cf8 = cache->dtype == KVW_DTYPE_FP8_E4M3;
+    cudaError_t e;
+#ifdef KVW_TEST_HOOKS
+    if (withhold)
+        e = cf8 ? launch_dynamic<true, true>(a, out_scales, stream)
+                : launch_dynamic<false, true>(a, out_scales, stream);
+    else
+#else
+    if (withhold) return KVW_EUNSUPPORTED;
+#endif
+        e = cf8 ? launch_dynamic<true>(a, out_scales, stream)
+                : launch_dynamic<false>(a, out_scales, stream);
     return e == cudaSuccess ? KVW_OK : KVW_ECUDA;
 }
+
+}  // namespace
+}  // namespace kvw
+
+extern "C" int kvw_mla_gather_latent_fp8_dynamic(void* out_codes, float* out_scales,
+                                                 const kvw_paged_cache_t* cache,
+                                                 uint32_t layer_idx, const uint32_t* ctx_offsets,
+                                                 uint32_t num_batches, uint32_t total_rows,
+                                                 uint32_t* err_flags, cudaStream_t stream) {
+    return kvw::gather_dynamic_entry(out_codes, out_scales, cache, layer_idx, ctx_offsets,
+                                     num_batches, total_rows, err_flags, stream, false,
+                                     kvw::kWaitLimitNs);
+}
+
+#ifdef KVW_TEST_HOOKS
+// Test builds only (compiled with -DKVW_TEST_HOOKS into a separate library;
+// the product library has no such symbol): the dynamic-FP8 gather with the
+// first step of every warp announced on its stage barrier but never copied,
+// and every wait bounded by `wait_ns`, so each warp's first wait runs out,
+// KVW_ERR_TIMEOUT is set and the kernel returns without writing a row.
+extern "C" int kvw_test_gather_dynamic_withheld_stage(void* out_codes, float* out_scales,
+                                                      const kvw_paged_cache_t* cache,
+                                                      uint32_t layer_idx,
+                                                      const uint32_t* ctx_offsets,
+                                                      uint32_t num_batches, uint32_t total_rows,
+                                                      uint32_t* err_flags, cudaStream_t stream,
+                                                      uint64_t wait_ns) {
+    return kvw::gather_dynamic_entry(out_codes, out_scales, cache, layer_idx, ctx_offsets,
+                                     num_batches, total_rows, err_flags, stream, true, wait_ns);
+}
+#endif
