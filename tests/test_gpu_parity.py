@@ -409,9 +409,18 @@ def test_knorm_full_with_bad_pages(orc, dev, G):
 
 # ------------------------------------------------------------ padded layouts, small batches
 
-@pytest.mark.parametrize("kind", ["mla", "gqa", "gqa_mrope", "knorm"])
+@pytest.mark.parametrize("kind", ["mla", "gqa", "gqa_mrope", "knorm", "gather", "gather_dynamic",
+                                  "gather_dynamic_fp8"])
 def test_padded_cache_layouts(orc, dev, kind):
-    if kind == "mla":
+    if kind.startswith("gather"):
+        # padded rows: every latent row is copied from its own strided slot
+        f8 = kind.endswith("fp8")
+        w = W.mla_workload("p", 704, [3, 17, 1], [0, 40, 300], num_heads=1, page_size=16,
+                           max_seq_len=512, cache_dtype=W.DTYPE_FP8_E4M3 if f8 else W.DTYPE_BF16,
+                           num_layers=2, layer_idx=1, scale=1.0)
+        w.cache = W.repad_cache(w.cache, 16, 32)
+        run_gather(orc, dev, W.mla_gather(w, dynamic=kind != "gather"))
+    elif kind == "mla":
         w = W.mla_workload("p", 701, [3, 17, 1], [0, 40, 300], num_heads=16, page_size=16,
                            max_seq_len=512, cache_dtype=W.DTYPE_BF16, num_layers=2, layer_idx=1)
         w.cache = W.repad_cache(w.cache, 64, 0)
@@ -722,6 +731,22 @@ def test_gather_dynamic_every_bf16_maximum(orc, dev):
     assert is_nan.sum() == np.count_nonzero((rows & 0x7FFF) == 0x7F80)
     assert np.array_equal(got[~is_nan], ref[~is_nan])
     assert np.all((got[is_nan] & 0x7F) == 0x7F)
+
+
+@pytest.mark.parametrize("dynamic", [False, True])
+def test_gather_most_requests(orc, dev, dynamic):
+    """KVW_MAX_BATCHES requests of 0-5 context rows each: the staged offsets
+    take 32 KiB of shared memory beside the stages, and the steps of a warp
+    straddle many requests."""
+    n = 8192
+    rng = np.random.default_rng(890)
+    prior = rng.integers(0, 5, size=n)
+    new = (rng.random(n) < 0.5).astype(np.int64)
+    w = W.mla_workload("gb", 891, new, prior, num_heads=1, page_size=4, max_seq_len=8,
+                       cache_dtype=W.DTYPE_BF16)
+    g = W.mla_gather(w, dynamic=dynamic)
+    assert g.ctx_offsets.shape[0] - 1 == n and g.rows > 16000
+    run_gather(orc, dev, g)
 
 
 def test_gather_dynamic_prefill_full(orc, dev):
