@@ -36,9 +36,14 @@ def dev():
     return device
 
 
-def run_mla(orc, dev, w, **kw):
+def _launch(d, **kw):
+    """One call of the entry point a device holder wraps, on the current stream."""
+    d.run(**kw)
+
+
+def run_mla(orc, dev, w, launch=None, **kw):
     d = dev.DeviceMLA(w)
-    d.run()
+    (launch or _launch)(d)
     import torch
 
     torch.cuda.synchronize()
@@ -238,11 +243,11 @@ def test_mla_decode_identity_flags(orc, dev):
 
 # ------------------------------------------------------------------ GQA
 
-def run_gqa(orc, dev, w, alias=False):
+def run_gqa(orc, dev, w, alias=False, launch=None):
     import torch
 
     d = dev.DeviceGQA(w, alias_output=alias)
-    d.run()
+    (launch or _launch)(d)
     torch.cuda.synchronize()
     out0 = w.q_proj.copy() if alias else d.out_init.copy()
     if alias:
@@ -317,11 +322,11 @@ def test_gqa_error_flags(orc, dev):
 
 # ------------------------------------------------------------------ K norm
 
-def run_knorm(orc, dev, w, per_head_norm=True):
+def run_knorm(orc, dev, w, per_head_norm=True, launch=None):
     import torch
 
     d = dev.DeviceKNorm(w)
-    d.run(per_head_norm=per_head_norm)
+    (launch or _launch)(d, per_head_norm=per_head_norm)
     torch.cuda.synchronize()
     c_ref, f_ref = orc.rms_norm_kv_cache_paged(w, per_head_norm=per_head_norm, nthreads=NTHREADS)
     assert d.guards_intact()
@@ -568,11 +573,11 @@ def test_mla_inplace_flags(orc, dev):
 
 # ------------------------------------------------------------ paged -> contiguous gather
 
-def run_gather(orc, dev, g):
+def run_gather(orc, dev, g, launch=None):
     import torch
 
     d = dev.DeviceGather(g)
-    d.run()
+    (launch or _launch)(d)
     torch.cuda.synchronize()
     if g.dynamic:
         ref, ref_scales, f_ref = orc.mla_gather_latent_dynamic(
