@@ -754,6 +754,20 @@ def test_gather_most_requests(orc, dev, dynamic):
     run_gather(orc, dev, g)
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.75])
+def test_gather_dynamic_prefill_size_fp8_cache(orc, dev, scale):
+    """Prefill-size contexts (16 requests of 512-8192 rows) from an E4M3 cache:
+    at cache scale 1 the values are bf16 numbers and divide through the
+    refined quotient, at 0.75 through the IEEE divide; codes and scales bit
+    for bit."""
+    new = np.random.default_rng(1407).integers(512, 8192, size=16, endpoint=True)
+    w = W.mla_workload("gpf", 1408, new, np.zeros(16, np.int64), num_heads=1, page_size=128,
+                       max_seq_len=16384, cache_dtype=W.DTYPE_FP8_E4M3, scale=scale)
+    g = W.mla_gather(w, dynamic=True)
+    assert g.rows > 40000
+    run_gather(orc, dev, g)
+
+
 def test_gather_dynamic_prefill_full(orc, dev):
     run_gather(orc, dev, W.REGISTRY["mla_gather_prefill_dynamic"][0](2))
 
