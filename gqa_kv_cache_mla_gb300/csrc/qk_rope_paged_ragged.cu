@@ -722,10 +722,14 @@ int qk_entry(const void* q_proj, const uint32_t* input_row_offsets, uint32_t num
     // average one (for 40 heads of 128: 10 tokens x 3 slices use 0.89 of the
     // consumers, 11 tokens x 2 slices 0.69).  Larger groups cost less
     // producer work per token, so take the largest group whose use is at
-    // least 0.85, else the group size of the best use.
+    // least 0.85, else the group size of the best use; among equal uses, the
+    // largest group that leaves no consumer thread idle (40 heads of 128 with
+    // an E4M3 K cache: 4 tokens x 12 slices rather than 5 x 9, which idles 24
+    // of 384 threads; 2.5% faster in a same-box A/B).
     const uint32_t G_ = S / 16, H_ = num_q_heads + a.Hk;
     uint64_t tpb = tpb_max;
     double best = -1.0;
+    bool best_full = false;
     for (uint64_t c = tpb_max; c >= 1; --c) {
         uint64_t sl = kConsumers / (c * G_);
         if (sl < 1) sl = 1;
@@ -739,8 +743,10 @@ int qk_entry(const void* q_proj, const uint32_t* input_row_offsets, uint32_t num
             tpb = c;
             break;
         }
-        if (use > best + 1e-9) {
-            best = use;
+        const bool full = units == passes * kConsumers;
+        if (use > best + 1e-9 || (use > best - 1e-9 && full && !best_full)) {
+            if (use > best) best = use;
+            best_full = full;
             tpb = c;
         }
     }
