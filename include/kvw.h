@@ -39,9 +39,9 @@
  *     KVW_ERR_OFFSETS  input_row_offsets does not start at 0, does not end
  *                      at the token count, or decreases: nothing is written.
  *     KVW_ERR_TIMEOUT  an internal pipeline wait (between the copy engine
- *                      and the compute warps of one CTA of the GQA kernel)
- *                      gave up after about one second of GPU time; the
- *                      output is incomplete.  Reported instead of hanging
+ *                      and the compute warps of the GQA kernel or of the
+ *                      dynamic-FP8 latent gather) gave up after about one
+ *                      second of GPU time; the output is incomplete.  Reported instead of hanging
  *                      the GPU.  It is not expected on a healthy device, but
  *                      a CTA that the GPU pre-empts for longer than the
  *                      limit (time slicing with other processes on a shared
@@ -226,7 +226,9 @@ int kvw_mla_gather_latent(void* out, int32_t out_dtype, float out_scale,
  *   out_codes    device, uint8 [total_rows, 576], 16-byte aligned
  *   out_scales   device, f32 [total_rows]
  *   other arguments, flags and errors as kvw_mla_gather_latent; a row
- *   without a valid page is not written (neither codes nor scale).
+ *   without a valid page is not written (neither codes nor scale).  The
+ *   rows reach the compute warps through bounded pipeline waits, so this
+ *   call can also report KVW_ERR_TIMEOUT (see the flags above).
  */
 int kvw_mla_gather_latent_fp8_dynamic(void* out_codes, float* out_scales,
                                       const kvw_paged_cache_t* cache, uint32_t layer_idx,
