@@ -414,7 +414,8 @@ cudaError_t launch_rows_for(const KnArgs& a, size_t smem, uint32_t pt_words, cud
     if (a.nv <= 16) return launch_rows<4, 4, 2, MBC>(a, smem, pt_words, stream);
     if (a.nv <= 32) return launch_rows<8, 4, 2, MBC>(a, smem, pt_words, stream);
     if (a.nv <= 64) return launch_rows<16, 4, 2, MBC>(a, smem, pt_words, stream);
-    return launch_rows<32, 4, 1, MBC>(a, smem, pt_words, stream);
+    // whole K rows (up to 1024 columns): two rows per team measured 11% faster than one
+    return launch_rows<32, 4, 2, MBC>(a, smem, pt_words, stream);
 }
 
 template <int VPL, int RPT, bool MBC, bool FULL>
