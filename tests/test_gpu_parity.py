@@ -123,6 +123,33 @@ def test_mla_many_requests_and_page_size_one(orc, dev):
     run_mla(orc, dev, w)
 
 
+@pytest.mark.parametrize("kind", ["gqa", "gqa_fp8k", "gqa_mrope", "knorm64", "knorm_row",
+                                  "gather", "gather_dynamic"])
+def test_page_size_one(orc, dev, kind):
+    """Pages of one token: every row of a request sits on its own page, so
+    consecutive rows are never adjacent and every slot lookup is distinct."""
+    rng = np.random.default_rng(1501)
+    B = 300
+    new = rng.integers(0, 4, B)
+    prior = rng.integers(0, 40, B)
+    if kind.startswith("gqa"):
+        mode = "mrope" if kind == "gqa_mrope" else None
+        w = W.gqa_workload("p1", 1502, new, prior, 8, 2, 64, page_size=1, freqs_rows=64,
+                           base=10000.0, interleaved=kind != "gqa_mrope", position_mode=mode,
+                           mrope_section=(8, 12, 12) if mode else None,
+                           cache_dtype=W.DTYPE_FP8_E4M3 if kind == "gqa_fp8k" else W.DTYPE_BF16)
+        run_gqa(orc, dev, w)
+    elif kind.startswith("knorm"):
+        per_head = kind == "knorm64"
+        w = W.knorm_workload("p1", 1503, new, prior, 2, 128, page_size=1,
+                             gamma_len=64 if per_head else 256)
+        run_knorm(orc, dev, w, per_head_norm=per_head)
+    else:
+        w = W.mla_workload("p1", 1504, new, prior, num_heads=1, page_size=1, max_seq_len=64,
+                           cache_dtype=W.DTYPE_BF16)
+        run_gather(orc, dev, W.mla_gather(w, dynamic=kind == "gather_dynamic"))
+
+
 def test_mla_error_flags(orc, dev):
     # position past the table
     w = W.mla_workload("p", 91, [2, 5], [0, 60], num_heads=2, page_size=16, max_seq_len=80,
