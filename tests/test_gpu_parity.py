@@ -150,6 +150,36 @@ def test_page_size_one(orc, dev, kind):
         run_gather(orc, dev, W.mla_gather(w, dynamic=kind == "gather_dynamic"))
 
 
+@pytest.mark.parametrize("page", [3, 12, 48, 100])
+@pytest.mark.parametrize("kind", ["mla", "gqa", "knorm", "gather_dynamic"])
+def test_page_sizes_not_powers_of_two(orc, dev, kind, page):
+    """Page sizes with no power-of-two factor to shift by: the kernels divide
+    slot positions by the page size through multiply-high constants, which
+    must give the exact quotient and remainder for every position."""
+    rng = np.random.default_rng(1600 + page)
+    B = 40
+    new = rng.integers(0, 40, B)
+    prior = rng.integers(0, 400, B)
+    max_seq = int(-(-int((new + prior).max() + 1) // page) * page)
+    if kind == "mla":
+        w = W.mla_workload("pp", 1601 + page, new, prior, num_heads=3, page_size=page,
+                           max_seq_len=max_seq, cache_dtype=W.DTYPE_FP8_E4M3, num_layers=2,
+                           layer_idx=1)
+        run_mla(orc, dev, w)
+    elif kind == "gqa":
+        w = W.gqa_workload("pp", 1602 + page, new, prior, 8, 2, 128, page_size=page,
+                           freqs_rows=max_seq, base=500000.0, interleaved=True)
+        run_gqa(orc, dev, w)
+    elif kind == "knorm":
+        w = W.knorm_workload("pp", 1603 + page, new, prior, 3, 128, page_size=page,
+                             gamma_len=64)
+        run_knorm(orc, dev, w)
+    else:
+        w = W.mla_workload("pp", 1604 + page, new, prior, num_heads=1, page_size=page,
+                           max_seq_len=max_seq, cache_dtype=W.DTYPE_BF16)
+        run_gather(orc, dev, W.mla_gather(w, dynamic=True))
+
+
 def test_mla_error_flags(orc, dev):
     # position past the table
     w = W.mla_workload("p", 91, [2, 5], [0, 60], num_heads=2, page_size=16, max_seq_len=80,
